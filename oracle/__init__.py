@@ -47,8 +47,5 @@ from .attention import (  # noqa: F401
 from .accounting import (  # noqa: F401
     token_counts,
     attended_pairs,
-    attention_flops,
-    pack_bytes,
-    reconstruct_bytes,
     batch_stats,
 )

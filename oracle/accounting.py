@@ -44,26 +44,6 @@ def attended_pairs(prompt_lens, resp_lens_per_group, duplicated=False):
     return pairs
 
 
-def attention_flops(pairs, Hq, D):
-    """Useful FLOPs: forward = 2 GEMMs (QK^T and PV) = 4*D FLOPs per pair per
-    query head; backward = 5 GEMMs = 10*D per pair per query head."""
-    fwd = 4 * D * Hq * pairs
-    bwd = 10 * D * Hq * pairs
-    return fwd, bwd
-
-
-def pack_bytes(T, W, elem_bytes):
-    """Algorithmic bytes of packing a [B,L,W] row tensor: every packed row is
-    read once and written once."""
-    return 2 * T * W * elem_bytes
-
-
-def reconstruct_bytes(T, B, L, W, elem_bytes):
-    """Algorithmic bytes of reconstruction: each packed row read once, every
-    output row of [B,L,W] written once."""
-    return (T + B * L) * W * elem_bytes
-
-
 def batch_stats(attention_mask, response_length):
     """Statistics of a normal (not deduplicated) batch from its attention mask
     ("Debugging & Analysis", "Batch Statistics": prompt length, response count
