@@ -4,8 +4,10 @@ One step = the whole path on one synthetic batch: find prompt groups, pack ids,
 positions and the [B, L, 1024] hidden states, split attention forward and
 backward on the packed Q/K/V/dO, and reconstruct the attention output back to
 [B, L, Hq*D].  The headline value is useful split-attention fwd+bwd TFLOP/s
-(attended pairs only) over the whole step; pack/reconstruct GB/s and the
-per-kernel roofline are reported beside it.
+(attended pairs only) over the whole step, on the long-context workload (4
+prompts of 32768 tokens x 8 responses of 2048, the largest configuration);
+unique tokens per second, pack/reconstruct GB/s, the per-kernel roofline and
+the same figures for every other configuration are reported beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
@@ -15,7 +17,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -33,31 +34,51 @@ from dummy_batch import WORKLOADS, make_workload_batch, make_qkv, make_rows, bf1
 
 METRIC = "split-attn fwd+bwd useful TFLOP/s (% BF16 peak); pack/reconstruct GB/s"
 UNIT = "TFLOP/s"
-DEFAULT_WORKLOAD = "worked_example"
+DEFAULT_WORKLOAD = "long_context"
+# the other configurations, measured in the same run and reported by name
+# (workload, use_unpad)
+EXTRA_WORKLOADS = [("worked_example", False), ("qwen3_0p6b", False), ("pipeline", False),
+                   ("pipeline", True), ("pipeline_nodedup", False)]
 HIDDEN = 1024  # Qwen3-0.6B hidden size: the row width packed in every step
 
+# Algorithmic FLOPs of the attention kernels per attended (query, key) pair,
+# per query head and per unit of head_dim: a GEMM over the pairs costs 2 D.
+KERNEL_FLOPS_PER_PAIR = {
+    "attn_fwd": 4,    # S = Q K^T, O = P V
+    "attn_dkdv": 8,   # S^T, dP^T, dV += P^T dO, dK += dS^T Q
+    "attn_dq": 2,     # dQ += dS K (S and dP recomputed there are not counted)
+    "attn_bwd": 10,   # the fused backward: S^T, dP^T, dV, dK and dQ
+}
+KERNEL_NAMES = {
+    "attn_fwd": "attn_fwd_tc_kernel (split-attention forward)",
+    "attn_dkdv": "attn_dkdv_tc_kernel (split-attention backward, dK and dV)",
+    "attn_dq": "attn_dq_tc_kernel (split-attention backward, dQ)",
+    "attn_bwd": "attn_bwd_tc_kernel (split-attention backward, dK, dV and dQ)",
+}
 
-def parse():
+
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--attn-impl", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--unpad", action="store_true", help="pack with use_unpad (needs a mask)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-standard", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other configurations")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
-def workload_desc(wl):
+def workload_desc(wl, use_unpad=False):
     resp = f"{wl.R}" if wl.resp_len_range is None else \
         f"{wl.resp_len_range[0]}..{wl.resp_len_range[1]} right-padded to {wl.R}"
-    return (f"{wl.name}: {wl.G} unique prompt(s) x {wl.n} responses (B={wl.B}), prompt {wl.P}, "
-            f"response {resp}; {wl.Hq} Q / {wl.Hkv} KV heads, head_dim {wl.D}, {wl.dtype}; "
-            f"hidden {HIDDEN} packed")
+    return (f"{wl.name}{' (unpadded)' if use_unpad else ''}: {wl.G} unique prompt(s) x {wl.n} responses "
+            f"(B={wl.B}), prompt {wl.P}, response {resp}; {wl.Hq} Q / {wl.Hkv} KV heads, head_dim {wl.D}, "
+            f"{wl.dtype}; {'forward + backward' if wl.backward else 'forward only'}; hidden {HIDDEN} packed")
 
 
 def useful_pairs(info):
@@ -125,19 +146,21 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, mx, reasons = [], None, set()
+        sm, mx, power, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         window = self.samples[begin:None if end is None else end + 1] or self.samples
         for s in window:
             try:
                 sm.append(float(s[1]))
                 mx = float(s[2])
+                power.append(float(s[3]))
                 for i, n in enumerate(names):
                     if s[5 + i].lower().startswith("active"):
                         reasons.add(n)
             except (ValueError, IndexError):
                 continue
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "power_w_median": statistics.median(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -173,50 +196,103 @@ def kernel_source_digest(entry) -> str | None:
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when the kernel's source changed since the counters were taken."""
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/traffic.json), or None when the kernel's source changed
+    since the counters were taken.  A capture taken on a smaller case of the
+    same kernel is scaled by the entry's stated factor for this workload."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
     except (OSError, ValueError):
-        return None
+        return None, None
     e = t.get(kernel)
     if not e or kernel_source_digest(e) != e.get("kernel_sha256_16"):
-        return None
-    return e.get("bytes_per_launch_full")
+        return None, None
+    if e.get("workload") == workload:
+        return e.get("bytes_per_launch"), f"ncu capture on {workload}"
+    factor = e.get("scale_to", {}).get(workload)
+    if factor is None:
+        return None, None
+    return e["bytes_per_launch"] * factor, f"ncu capture on {e['workload']}, x{factor} ({e.get('scale_reason', '')})"
 
 
 # ------------------------------------------------------- oracle (CPU arm)
-def cpu_baseline(wl, seconds):
-    """The oracle as it stands, on a bounded sample of the workload: query rows
-    drawn uniformly from the packed batch, each row's split attention forward
-    and its exact backward (sparse upstream gradient), every head.  Returns
-    TFLOP/s of useful work and a description."""
+class OracleSample:
+    """The oracle as it stands, on a bounded sample of a workload: its batch,
+    packing and seeded Q/K/V/dO are prepared once; each timed sample draws
+    query rows uniformly from the packed batch and runs each row's split
+    attention forward and its exact backward (sparse upstream gradient),
+    every head."""
+
+    def __init__(self, wl, use_unpad=False):
+        import oracle
+        self.oracle, self.wl = oracle, wl
+        ids, mask, pos = make_workload_batch(wl, list(WORKLOADS).index(wl.name))
+        groups, uniq = oracle.find_prompt_groups(ids, wl.R, mask)
+        _, _, self.info = oracle.create_deduplicated_batch(ids, pos, wl.R, groups, uniq, attention_mask=mask,
+                                                           use_unpad=use_unpad)
+        self.q, self.k, self.v, self.do = make_qkv(self.info.T, wl.Hq, wl.Hkv, wl.D, 7)
+        self.keysets = oracle.row_key_sets(self.info)
+        self.valid_rows = np.flatnonzero(self.info.row_valid)
+        self.rng = np.random.default_rng(0)
+        self.per_row = (4.0 + 10.0) if wl.backward else 4.0
+        self.cores = os.cpu_count()
+
+    def run(self, seconds):
+        """TFLOP/s of useful work over about `seconds` of sampled rows, and a
+        description of the sample."""
+        wl, oracle = self.wl, self.oracle
+        flops = 0.0
+        rows_done = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            rows = [int(self.valid_rows[int(i)]) for i in self.rng.integers(0, len(self.valid_rows), size=4)]
+            oracle.split_attention_fwd_rows(self.q, self.k, self.v, self.info, rows, key_sets=self.keysets)
+            if wl.backward:
+                oracle.split_attention_bwd_sparse(self.q, self.k, self.v, self.do, self.info, rows,
+                                                  key_sets=self.keysets)
+            flops += sum(len(self.keysets[r]) for r in rows) * self.per_row * wl.D * wl.Hq
+            rows_done += len(rows)
+        el = time.perf_counter() - t0
+        return flops / el / 1e12, (f"oracle (fp64 NumPy) split attention "
+                                   f"{'fwd + exact bwd' if wl.backward else 'fwd'} on {rows_done} uniformly drawn "
+                                   f"query rows x {wl.Hq} heads of the {wl.name} batch, {el:.1f} s; {self.cores} "
+                                   f"host cores available to NumPy's BLAS")
+
+
+def cpu_baseline(wl, seconds, use_unpad=False):
+    """One bounded oracle sample of the workload: (TFLOP/s, cores, description)."""
+    o = OracleSample(wl, use_unpad)
+    v, desc = o.run(seconds)
+    return v, o.cores, desc
+
+
+def oracle_copy_times(wl, use_unpad=False, cols=64):
+    """The oracle's grouping and packing of ids and positions, timed on the full
+    batch; its row pack of the hidden states and its reconstruction of the
+    attention output, timed on the full row set at `cols` float32 columns and
+    scaled by width to the real rows (HIDDEN and Hq*D columns).  Seconds."""
     import oracle
     ids, mask, pos = make_workload_batch(wl, list(WORKLOADS).index(wl.name))
-    groups, uniq = oracle.find_prompt_groups(ids, wl.R, mask)
-    _, _, info = oracle.create_deduplicated_batch(ids, pos, wl.R, groups, uniq, attention_mask=mask)
-    q, k, v, do = make_qkv(info.T, wl.Hq, wl.Hkv, wl.D, 7)
-    keysets = oracle.row_key_sets(info)
-    valid_rows = [t for t in range(info.T) if info.row_valid[t]]
-    rng = np.random.default_rng(0)
-    flops = 0.0
-    rows_done = 0
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds:
-        rows = [valid_rows[int(i)] for i in rng.integers(0, len(valid_rows), size=4)]
-        oracle.split_attention_fwd_rows(q, k, v, info, rows, key_sets=keysets)
-        oracle.split_attention_bwd_sparse(q, k, v, do, info, rows, key_sets=keysets)
-        flops += sum(len(keysets[r]) for r in rows) * 14.0 * wl.D * wl.Hq
-        rows_done += len(rows)
-    el = time.perf_counter() - t0
-    cores = os.cpu_count()
-    return flops / el / 1e12, cores, (f"oracle (fp64 NumPy) split attention fwd + exact bwd on {rows_done} "
-                                      f"uniformly drawn query rows x {wl.Hq} heads of the {wl.name} batch, "
-                                      f"{el:.1f} s; group/pack/reconstruct not included; "
-                                      f"{cores} host cores available to NumPy's BLAS")
+    groups, uniq = oracle.find_prompt_groups(ids, wl.R, mask)
+    t1 = time.perf_counter()
+    _, _, info = oracle.create_deduplicated_batch(ids, pos, wl.R, groups, uniq, attention_mask=mask,
+                                                  use_unpad=use_unpad)
+    t2 = time.perf_counter()
+    rows = np.zeros((wl.B, wl.L, cols), dtype=np.float32)
+    oracle.pack_rows(rows, info)
+    t3 = time.perf_counter()
+    oracle.reconstruct_sequences(np.zeros((info.T, cols), dtype=np.float32), info)
+    t4 = time.perf_counter()
+    return {"group_s": t1 - t0, "pack_ids_positions_s": t2 - t1,
+            "pack_hidden_s_extrapolated": (t3 - t2) * HIDDEN / cols,
+            "reconstruct_s_extrapolated": (t4 - t3) * (wl.Hq * wl.D) / cols,
+            "note": f"group and ids/positions pack timed in full; hidden pack and reconstruction timed on "
+                    f"every row at {cols} float32 columns and scaled by width to {HIDDEN} and {wl.Hq * wl.D} "
+                    f"columns (extrapolated)"}
 
 
 def run_reference(args):
@@ -224,19 +300,35 @@ def run_reference(args):
     if rank != 0:
         return
     wl = WORKLOADS[args.workload]
-    per = max(args.cpu_seconds / max(args.steps + args.warmup, 1), 1.0)
+    use_unpad = bool(getattr(args, "unpad", False))
+    per = max(args.cpu_seconds / max(args.steps + args.warmup, 1), 0.5)
+    sample = OracleSample(wl, use_unpad)
     vals = []
-    desc = cores = None
+    desc = None
     for i in range(args.warmup + args.steps):
-        v, cores, desc = cpu_baseline(wl, per)
+        v, desc = sample.run(per)
         if i >= args.warmup:
             vals.append(v)
     value = statistics.median(vals)
+    cores = sample.cores
+    # the oracle's time for one whole step, extrapolated: the attention's useful
+    # FLOPs at the sampled rate, plus the copy steps (timed, or scaled by width)
+    import oracle
+    info = sample.info
+    pairs = oracle.attended_pairs([int(info.prompt_len[g]) for g in range(info.G)],
+                                  [[int(info.resp_len[b]) for b in grp] for grp in info.prompt_groups])
+    attn_flops = ((4.0 + 10.0) if wl.backward else 4.0) * wl.D * wl.Hq * pairs
+    copies = oracle_copy_times(wl, use_unpad)
+    attn_s = attn_flops / (value * 1e12)
+    step_s = attn_s + copies["group_s"] + copies["pack_ids_positions_s"] + \
+        copies["pack_hidden_s_extrapolated"] + copies["reconstruct_s_extrapolated"]
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(wl)},
+            "ms_per_step": step_s * 1e3, "ms_per_step_kind": "extrapolated (see oracle_step)",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(wl, use_unpad)},
+            "oracle_step": {"attention_s_extrapolated": attn_s, "attention_flops": attn_flops,
+                            "useful_pairs_per_head": pairs, "sample_seconds_per_step": per, **copies},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -256,6 +348,137 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+PHASES = ("group", "pack", "pack_hidden", "fwd", "bwd", "recon")
+
+
+class Case:
+    """One configuration on the device: its batch, persistent buffers and the
+    whole-path step through the public binding."""
+
+    def __init__(self, zr, wl, dev, use_unpad=False):
+        import torch
+        self.zr, self.wl, self.dev, self.use_unpad = zr, wl, dev, use_unpad
+        idx = list(WORKLOADS).index(wl.name)
+        self.ids_np, self.mask_np, self.pos_np = make_workload_batch(wl, idx)
+        R = wl.R
+        t_ids = torch.from_numpy(self.ids_np).to(dev)
+        t_mask = None if self.mask_np is None else torch.from_numpy(self.mask_np).to(dev)
+        t_pos = torch.from_numpy(self.pos_np).to(dev)
+        self.t_ids, self.t_mask, self.t_pos = t_ids, t_mask, t_pos
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(500 + idx)
+        self.t_hidden = torch.randn((wl.B, wl.L, HIDDEN), generator=gen, device=dev, dtype=torch.float32).to(
+            torch.bfloat16)
+        # T from one untimed pass (sizes the packed buffers exactly)
+        g = zr.find_prompt_groups(t_ids, R, t_mask, sync=True)
+        _, _, _, info0, T = zr.pack_dedup(t_ids, t_pos, R, g, t_mask, use_unpad=use_unpad, sync=True)
+        arrays = info0.arrays()
+        self.G = arrays["num_groups"]
+        self.pairs = useful_pairs(arrays)
+        self.T = T
+        self.fwd_flops = 4.0 * wl.D * wl.Hq * self.pairs
+        self.bwd_flops = 10.0 * wl.D * wl.Hq * self.pairs if wl.backward else 0.0
+        self.attn_flops = self.fwd_flops + self.bwd_flops
+        T_cap = T
+        self.T_cap = T_cap
+        gen.manual_seed(900 + idx)
+        self.tq, self.tk, self.tv, self.tdo = (
+            torch.randn((T_cap, h, wl.D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            for h in (wl.Hq, wl.Hkv, wl.Hkv, wl.Hq))
+        self.groups = zr.Groups(wl.B, dev)
+        self.groups.unique_prompts = torch.empty((wl.B, wl.P), dtype=torch.int64, device=dev)
+        self.grp_ws = zr._aligned_empty(zr.lib().zr_find_prompt_groups_workspace(wl.B, wl.L), dev)
+        self.info = zr.ReconInfo(wl.B, wl.L, R, use_unpad, T_cap, dev)
+        self.ids_out = torch.empty(T_cap, dtype=torch.int64, device=dev)
+        self.pos_out = torch.empty(T_cap, dtype=torch.int64, device=dev)
+        self.hid_out = torch.empty((T_cap, HIDDEN), dtype=torch.bfloat16, device=dev)
+        self.attn_ws = zr.attn_workspace(self.info, wl.Hq, wl.Hkv, wl.D, dev)
+        self.o = torch.empty_like(self.tq)
+        self.lse = torch.empty((T_cap, wl.Hq), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = torch.empty_like(self.tq), torch.empty_like(self.tk), torch.empty_like(self.tv)
+        self.recon = torch.empty((wl.B, wl.L, wl.Hq * wl.D), dtype=torch.bfloat16, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def step(self, ev=None, inputs=None, outputs=None):
+        """The whole path once.  `ev` maps phase -> (start, end) events;
+        `inputs` / `outputs` replace the resident tensors (end-to-end run)."""
+        zr, wl = self.zr, self.wl
+        ids, pos, mask, hidden, q, k, v, do = inputs or (self.t_ids, self.t_pos, self.t_mask, self.t_hidden,
+                                                         self.tq, self.tk, self.tv, self.tdo)
+        dq, dk, dv, recon = outputs or (self.dq, self.dk, self.dv, self.recon)
+
+        def mark(name, i):
+            if ev is not None:
+                ev[name][i].record(self.stream)
+        mark("group", 0)
+        zr.find_prompt_groups(ids, wl.R, mask, workspace=self.grp_ws, out=self.groups)
+        mark("group", 1)
+        mark("pack", 0)
+        zr.pack_dedup(ids, pos, wl.R, self.groups, mask, use_unpad=self.use_unpad, info=self.info,
+                      out=(self.ids_out, self.pos_out, None))
+        mark("pack", 1)
+        mark("pack_hidden", 0)
+        zr.pack_rows(self.info, hidden, out=self.hid_out)
+        mark("pack_hidden", 1)
+        mark("fwd", 0)
+        zr.split_attn_fwd(self.info, q, k, v, workspace=self.attn_ws, out=(self.o, self.lse))
+        mark("fwd", 1)
+        mark("bwd", 0)
+        if wl.backward:
+            zr.split_attn_bwd(self.info, q, k, v, self.o, self.lse, do, workspace=self.attn_ws, out=(dq, dk, dv))
+        mark("bwd", 1)
+        mark("recon", 0)
+        zr.reconstruct(self.info, self.o.view(self.T_cap, wl.Hq * wl.D), out=recon)
+        mark("recon", 1)
+
+    def measure(self, steps, warmup, flush, on_start=None):
+        """Median phase times and the mean whole-step time (ms) over `steps`
+        timed steps after `warmup` untimed ones; L2 flushed before every step,
+        outside the timed events."""
+        import torch
+        ev = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in PHASES}
+        for _ in range(warmup):
+            flush.zero_()
+            self.step()
+        torch.cuda.synchronize()
+        self.zr.check_status(self.info, self.attn_ws)
+        if on_start:
+            on_start()
+        times = {n: [] for n in PHASES}
+        total = []
+        for _ in range(steps):
+            flush.zero_()
+            self.step(ev)
+            torch.cuda.synchronize()
+            for n, (a, b) in ev.items():
+                times[n].append(a.elapsed_time(b))
+            total.append(ev["group"][0].elapsed_time(ev["recon"][1]))
+        torch.cuda.synchronize()
+        self.zr.check_status(self.info, self.attn_ws)
+        return {n: statistics.median(v) for n, v in times.items()}, sum(total) / len(total)
+
+    def summary(self, med, ms_step, peaks, world=1):
+        """Throughput figures of one configuration."""
+        wl = self.wl
+        out = {"workload": workload_desc(wl, self.use_unpad), "B": wl.B, "L": wl.L, "T_packed": self.T,
+               "groups": self.G, "useful_pairs_per_head": self.pairs, "ms_per_step": ms_step,
+               "tflops_per_step": world * self.attn_flops / (ms_step * 1e-3) / 1e12,
+               "unique_tokens_per_s": world * self.T / (ms_step * 1e-3),
+               "batch_tokens_per_s": world * wl.B * wl.L / (ms_step * 1e-3),
+               "breakdown_ms": med}
+        out["frac_of_sustained_peak"] = out["tflops_per_step"] / (world * peaks["bf16_tflops_sustained"])
+        out["attn_fwd_tflops"] = self.fwd_flops / (med["fwd"] * 1e-3) / 1e12
+        if wl.backward:
+            out["attn_bwd_tflops"] = self.bwd_flops / (med["bwd"] * 1e-3) / 1e12
+        pack_bytes = 2 * self.T * HIDDEN * 2  # hidden rows: read once, written once
+        recon_bytes = (self.T + wl.B * wl.L) * wl.Hq * wl.D * 2
+        out["pack_hidden"] = {"bytes": pack_bytes, "gbs": pack_bytes / (med["pack_hidden"] * 1e-3) / 1e9}
+        out["pack_hidden"]["frac_of_measured_hbm"] = out["pack_hidden"]["gbs"] / peaks["hbm_gbs"]
+        out["reconstruct"] = {"bytes": recon_bytes, "gbs": recon_bytes / (med["recon"] * 1e-3) / 1e9}
+        out["reconstruct"]["frac_of_measured_hbm"] = out["reconstruct"]["gbs"] / peaks["hbm_gbs"]
+        return out
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
@@ -272,155 +495,76 @@ def run_native(args):
     __graft_entry__.build()
     from prompt_deduplicated_shared_gb300 import zr
 
-    if args.attn_impl != "auto":
-        zr.set_option("attn_impl", {"simt": 1, "tc": 2}[args.attn_impl])
-
+    peaks = load_peaks()
     wl = WORKLOADS[args.workload]
-    idx = list(WORKLOADS).index(wl.name)
     # every rank processes its own batch (groups are independent units)
-    ids_np, mask_np, pos_np = make_workload_batch(wl, idx)
-    hidden_np = bf16_round(make_rows(wl.B, wl.L, HIDDEN, 500 + idx))
-    R = wl.R
-    t_ids = torch.from_numpy(ids_np).to(dev)
-    t_mask = None if mask_np is None else torch.from_numpy(mask_np).to(dev)
-    t_pos = torch.from_numpy(pos_np).to(dev)
-    t_hidden = torch.from_numpy(hidden_np).to(dev, torch.bfloat16)
-
-    # T from one untimed pass (sizes the packed buffers exactly)
-    g = zr.find_prompt_groups(t_ids, R, t_mask, sync=True)
-    _, _, _, info, T = zr.pack_dedup(t_ids, t_pos, R, g, t_mask, sync=True)
-    info_arrays = info.arrays()
-    pairs = useful_pairs(info_arrays)
-    fwd_flops = 4.0 * wl.D * wl.Hq * pairs
-    bwd_flops = 10.0 * wl.D * wl.Hq * pairs
-    T_cap = T
-    q_np, k_np, v_np, do_np = (bf16_round(x) for x in make_qkv(T, wl.Hq, wl.Hkv, wl.D, 900 + idx))
-    tq, tk, tv, tdo = (torch.from_numpy(x).to(dev, torch.bfloat16) for x in (q_np, k_np, v_np, do_np))
-
-    # persistent buffers (allocated once, reused by every step)
-    groups = zr.Groups(wl.B, dev)
-    groups.unique_prompts = torch.empty((wl.B, wl.P), dtype=torch.int64, device=dev)
-    grp_ws = zr._aligned_empty(zr.lib().zr_find_prompt_groups_workspace(wl.B, wl.L), dev)
-    info = zr.ReconInfo(wl.B, wl.L, R, False, T_cap, dev)
-    ids_out = torch.empty(T_cap, dtype=torch.int64, device=dev)
-    pos_out = torch.empty(T_cap, dtype=torch.int64, device=dev)
-    hid_out = torch.empty((T_cap, HIDDEN), dtype=torch.bfloat16, device=dev)
-    attn_ws = zr.attn_workspace(info, wl.Hq, wl.Hkv, wl.D, dev)
-    o = torch.empty_like(tq)
-    lse = torch.empty((T_cap, wl.Hq), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
-    recon = torch.empty((wl.B, wl.L, wl.Hq * wl.D), dtype=torch.bfloat16, device=dev)
+    case = Case(zr, wl, dev, use_unpad=args.unpad)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
-    ev = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for n in ("group", "pack", "pack_hidden", "fwd", "bwd", "recon")}
-
-    def step(timed):
-        def mark(name, i):
-            if timed:
-                ev[name][i].record(stream)
-        mark("group", 0)
-        zr.find_prompt_groups(t_ids, R, t_mask, workspace=grp_ws, out=groups)
-        mark("group", 1)
-        mark("pack", 0)
-        zr.pack_dedup(t_ids, t_pos, R, groups, t_mask, info=info, out=(ids_out, pos_out, None))
-        mark("pack", 1)
-        mark("pack_hidden", 0)
-        zr.pack_rows(info, t_hidden, out=hid_out)
-        mark("pack_hidden", 1)
-        mark("fwd", 0)
-        zr.split_attn_fwd(info, tq, tk, tv, workspace=attn_ws, out=(o, lse))
-        mark("fwd", 1)
-        mark("bwd", 0)
-        zr.split_attn_bwd(info, tq, tk, tv, o, lse, tdo, workspace=attn_ws, out=(dq, dk, dv))
-        mark("bwd", 1)
-        mark("recon", 0)
-        zr.reconstruct(info, o.view(T_cap, wl.Hq * wl.D), out=recon)
-        mark("recon", 1)
-
-    for _ in range(args.warmup):
-        step(False)
-        flush.zero_()
-    torch.cuda.synchronize()
-    zr.check_status(info, attn_ws)
-
-    times = {n: [] for n in ev}
-    total = []
-    launches0 = zr.kernel_launches()
     clocks = ClockSampler()
     clocks.start()
-    zr.kernel_time_reset()
-    zr.set_option("kernel_timing", 1)  # per-kernel event pairs, for the roofline
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clock_begin = clocks.mark()
-    for _ in range(args.steps):
-        flush.zero_()  # L2 flush outside the timed events
-        step(True)
+    state = {}
+
+    def on_start():
+        zr.kernel_time_reset()
+        zr.set_option("kernel_timing", 1)  # per-kernel event pairs, for the roofline
+        state["launches0"] = zr.kernel_launches()
+        if world > 1:
+            dist.barrier()
         torch.cuda.synchronize()
-        st = 0.0
-        for n, (a, b) in ev.items():
-            t = a.elapsed_time(b)
-            times[n].append(t)
-            st += t
-        total.append(st)
-    torch.cuda.synchronize()
+        state["clock_begin"] = clocks.mark()
+
+    med, ms_local = case.measure(args.steps, args.warmup, flush, on_start=on_start)
     if world > 1:
         dist.barrier()
-    clock_info = clocks.stop(clock_begin, clocks.mark())
-    launches = zr.kernel_launches() - launches0
+    clock_info = clocks.stop(state["clock_begin"], clocks.mark())
+    launches = zr.kernel_launches() - state["launches0"]
     zr.set_option("kernel_timing", 0)
     kernel_ms = {}
-    for n in ("attn_fwd", "attn_bwd_prep", "attn_dkdv", "attn_dq", "pack_gather", "reconstruct"):
+    for n in ("attn_fwd", "attn_bwd_prep", "attn_bwd", "attn_dkdv", "attn_dq", "attn_dq_convert",
+              "pack_gather", "reconstruct"):
         tot, cnt = zr.kernel_time(n)
         if cnt:
             kernel_ms[n] = {"launches": cnt, "avg_ms": tot / cnt, "total_ms": tot}
     zr.kernel_time_reset()
-    zr.check_status(info, attn_ws)
-
-    ms_step = max_over_ranks(sum(total) / len(total), world, dev)
-    med = {n: statistics.median(v) for n, v in times.items()}
-    attn_flops = fwd_flops + bwd_flops
-    value = world * attn_flops / (ms_step * 1e-3) / 1e12
-
-    peaks = load_peaks()
     timed_total = sum(k["total_ms"] for k in kernel_ms.values())
     for k in kernel_ms.values():
         k["share_of_timed_kernels"] = k["total_ms"] / timed_total if timed_total else None
-    # dominant kernel: the dK/dV kernel of the backward.  Its algorithmic work
-    # is four GEMMs over the useful (query, key) pairs of every head: the
-    # recomputed scores S^T = K Q^T, dP^T = V dO^T, dV += P^T dO and
-    # dK += dS^T Q, i.e. 4 x 2 x D flops per pair and head.
-    dkdv_flops = 8.0 * wl.D * wl.Hq * pairs
-    dkdv_ms = kernel_ms["attn_dkdv"]["avg_ms"] if "attn_dkdv" in kernel_ms else float("nan")
-    dkdv_tflops = dkdv_flops / (dkdv_ms * 1e-3) / 1e12
-    bwd_tflops = bwd_flops / (med["bwd"] * 1e-3) / 1e12
-    fwd_tflops = fwd_flops / (med["fwd"] * 1e-3) / 1e12
-    pack_bytes = 2 * T * HIDDEN * 2  # hidden rows: read once, written once
-    recon_bytes = (T + wl.B * wl.L) * wl.Hq * wl.D * 2
-    pack_gbs = pack_bytes / (med["pack_hidden"] * 1e-3) / 1e9
-    recon_gbs = recon_bytes / (med["recon"] * 1e-3) / 1e9
+
+    ms_step = max_over_ranks(ms_local, world, dev)
+    value = world * case.attn_flops / (ms_step * 1e-3) / 1e12
+    summ = case.summary(med, ms_step, peaks, world)
+
+    # dominant kernel: the attention kernel with the largest share of the timed
+    # events; its algorithmic FLOPs per launch over its mean event time
+    attn_k = [n for n in kernel_ms if n in KERNEL_FLOPS_PER_PAIR]
+    dom = max(attn_k, key=lambda n: kernel_ms[n]["total_ms"])
+    dom_flops = KERNEL_FLOPS_PER_PAIR[dom] * wl.D * wl.Hq * case.pairs
+    dom_ms = kernel_ms[dom]["avg_ms"]
+    dom_tflops = dom_flops / (dom_ms * 1e-3) / 1e12
+    traffic, traffic_src = load_traffic(dom, wl.name if not args.unpad else wl.name + "_unpad")
+    kernel_tflops = {n: KERNEL_FLOPS_PER_PAIR[n] * wl.D * wl.Hq * case.pairs / (kernel_ms[n]["avg_ms"] * 1e-3) / 1e12
+                     for n in attn_k}
 
     # the reconstruction adjoint (backward through the reconstruction of the
     # attention output), timed on its own: it is not one of the steps above
-    grad_recon = torch.randn_like(recon)
-    grad_packed = torch.empty((T_cap, wl.Hq * wl.D), dtype=torch.bfloat16, device=dev)
+    grad_recon = torch.randn_like(case.recon)
+    grad_packed = torch.empty((case.T_cap, wl.Hq * wl.D), dtype=torch.bfloat16, device=dev)
     rb_times = []
     for i in range(args.warmup + 10):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        zr.reconstruct_backward(info, grad_recon, out=grad_packed)
-        b.record(stream)
+        a.record(case.stream)
+        zr.reconstruct_backward(case.info, grad_recon, out=grad_packed)
+        b.record(case.stream)
         torch.cuda.synchronize()
         if i >= args.warmup:
             rb_times.append(a.elapsed_time(b))
-    zr.check_status(info, attn_ws)
+    zr.check_status(case.info, case.attn_ws)
     rb_ms = statistics.median(rb_times)
-    rb_bytes = (wl.B * wl.L + T) * wl.Hq * wl.D * 2  # every output row read once, packed rows written
+    rb_bytes = (wl.B * wl.L + case.T) * wl.Hq * wl.D * 2  # every output row read once, packed rows written
     rb_gbs = rb_bytes / (rb_ms * 1e-3) / 1e9
+    del grad_recon, grad_packed
 
     # the standard strategy ("Split Attention Optimization", use_split_attention
     # off): reconstruct Q, K, V to the full sequences and run ordinary causal
@@ -429,9 +573,9 @@ def run_native(args):
     std = None
     if not args.no_standard:
         gi = zr.identity_groups(wl.B, dev)
-        _, _, _, info_id, T_id = zr.pack_dedup(t_ids, t_pos, R, gi, t_mask, sync=True)
-        qf, kf, vf, dof = (zr.reconstruct(info, x.view(T_cap, -1)).view(wl.B * wl.L, x.shape[1], wl.D)
-                           for x in (tq, tk, tv, tdo))
+        _, _, _, info_id, T_id = zr.pack_dedup(case.t_ids, case.t_pos, wl.R, gi, case.t_mask, sync=True)
+        qf, kf, vf, dof = (zr.reconstruct(case.info, x.view(case.T_cap, -1)).view(wl.B * wl.L, x.shape[1], wl.D)
+                           for x in (case.tq, case.tk, case.tv, case.tdo))
         ws_id = zr.attn_workspace(info_id, wl.Hq, wl.Hkv, wl.D, dev)
         of, lsef = torch.empty_like(qf), torch.empty((T_id, wl.Hq), dtype=torch.float32, device=dev)
         dqf, dkf, dvf = torch.empty_like(qf), torch.empty_like(kf), torch.empty_like(vf)
@@ -439,20 +583,21 @@ def run_native(args):
         for i in range(4):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
+            a.record(case.stream)
             zr.split_attn_fwd(info_id, qf, kf, vf, workspace=ws_id, out=(of, lsef))
-            zr.split_attn_bwd(info_id, qf, kf, vf, of, lsef, dof, workspace=ws_id, out=(dqf, dkf, dvf))
-            b.record(stream)
+            if wl.backward:
+                zr.split_attn_bwd(info_id, qf, kf, vf, of, lsef, dof, workspace=ws_id, out=(dqf, dkf, dvf))
+            b.record(case.stream)
             torch.cuda.synchronize()
             if i > 0:
                 st_times.append(a.elapsed_time(b))
         zr.check_status(info_id, ws_id)
         std_ms = statistics.median(st_times)
         split_ms = med["fwd"] + med["bwd"]
-        std = {"ms_attention_fwd_bwd": std_ms, "split_ms_attention_fwd_bwd": split_ms,
-               "speedup_of_split": std_ms / split_ms,
+        std = {"ms_attention": std_ms, "split_ms_attention": split_ms, "speedup_of_split": std_ms / split_ms,
                "note": "same kernels on the reconstructed full sequences, every row its own group"}
         del qf, kf, vf, dof, of, lsef, dqf, dkf, dvf, ws_id
+        torch.cuda.empty_cache()
 
     # end to end: host buffers in, results out, through the same public API.
     # Every step copies its inputs from pinned host memory and its results
@@ -461,14 +606,13 @@ def run_native(args):
     # upload and step i-1's download overlap step i's kernels.
     e2e = None
     if not args.no_e2e:
-        h_ids = torch.from_numpy(ids_np).pin_memory()
-        h_pos = torch.from_numpy(pos_np).pin_memory()
-        h_mask = None if mask_np is None else torch.from_numpy(mask_np).pin_memory()
-        h_hidden = t_hidden.cpu().pin_memory()
-        h_q, h_k, h_v, h_do = (x.cpu().pin_memory() for x in (tq, tk, tv, tdo))
-        h_in = [h_ids, h_pos, h_mask, h_hidden, h_q, h_k, h_v, h_do]
-        outs = [[torch.empty_like(x) for x in (dq, dk, dv, recon)] for _ in range(2)]
-        h_out = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dq, dk, dv, recon)]
+        h_ids = torch.from_numpy(case.ids_np).pin_memory()
+        h_pos = torch.from_numpy(case.pos_np).pin_memory()
+        h_mask = None if case.mask_np is None else torch.from_numpy(case.mask_np).pin_memory()
+        h_in = [h_ids, h_pos, h_mask] + [x.cpu().pin_memory() for x in
+                                         (case.t_hidden, case.tq, case.tk, case.tv, case.tdo)]
+        outs = [[torch.empty_like(x) for x in (case.dq, case.dk, case.dv, case.recon)] for _ in range(2)]
+        h_out = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (case.dq, case.dk, case.dv, case.recon)]
                  for _ in range(2)]
         d_in = [[None if x is None else torch.empty(x.shape, dtype=x.dtype, device=dev) for x in h_in]
                 for _ in range(2)]
@@ -481,7 +625,7 @@ def run_native(args):
         ev_out_ready = [torch.cuda.Event() for _ in range(2)]
         ev_out_free = [torch.cuda.Event() for _ in range(2)]
         for e in ev_in_free + ev_out_free:
-            e.record(stream)
+            e.record(case.stream)
 
         def e2e_step(i):
             j = i & 1
@@ -491,18 +635,11 @@ def run_native(args):
                     if h is not None:
                         d.copy_(h, non_blocking=True)
                 ev_in_ready[j].record(s_up)
-            d_ids, d_pos, d_mask, d_hidden, d_q, d_k, d_v, d_do = d_in[j]
-            e_dq, e_dk, e_dv, e_recon = outs[j]
-            stream.wait_event(ev_in_ready[j])
-            stream.wait_event(ev_out_free[j])
-            zr.find_prompt_groups(d_ids, R, d_mask, workspace=grp_ws, out=groups)
-            zr.pack_dedup(d_ids, d_pos, R, groups, d_mask, info=info, out=(ids_out, pos_out, None))
-            zr.pack_rows(info, d_hidden, out=hid_out)
-            zr.split_attn_fwd(info, d_q, d_k, d_v, workspace=attn_ws, out=(o, lse))
-            zr.split_attn_bwd(info, d_q, d_k, d_v, o, lse, d_do, workspace=attn_ws, out=(e_dq, e_dk, e_dv))
-            zr.reconstruct(info, o.view(T_cap, wl.Hq * wl.D), out=e_recon)
-            ev_in_free[j].record(stream)
-            ev_out_ready[j].record(stream)
+            case.stream.wait_event(ev_in_ready[j])
+            case.stream.wait_event(ev_out_free[j])
+            case.step(inputs=d_in[j], outputs=outs[j])
+            ev_in_free[j].record(case.stream)
+            ev_out_ready[j].record(case.stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(ev_out_ready[j])
                 for h, d in zip(h_out[j], outs[j]):
@@ -519,10 +656,29 @@ def run_native(args):
             e2e_step(i)
         t_end.record(s_down)
         torch.cuda.synchronize()
+        zr.check_status(case.info, case.attn_ws)
         ms_e2e = max_over_ranks(t_start.elapsed_time(t_end) / n_e2e, world, dev)
-        e2e = {"value": world * attn_flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+        e2e = {"value": world * case.attn_flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": ms_e2e, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "unique_tokens_per_s": world * case.T / (ms_e2e * 1e-3),
                "overlap": "uploads, kernels and downloads of consecutive steps overlap on separate streams"}
+        del h_in, outs, h_out, d_in
+    T_main = case.T
+    del case
+    torch.cuda.empty_cache()
+
+    # the other configurations, each its own whole-path step
+    extras = {}
+    if not args.no_extras:
+        for name, unpad in EXTRA_WORKLOADS:
+            if name == wl.name and unpad == args.unpad:
+                continue
+            c = Case(zr, WORKLOADS[name], dev, use_unpad=unpad)
+            m, ms = c.measure(max(5, min(args.steps, 10)), args.warmup, flush)
+            ms = max_over_ranks(ms, world, dev)
+            extras[name + ("_unpad" if unpad else "")] = c.summary(m, ms, peaks, world)
+            del c
+            torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
@@ -531,39 +687,49 @@ def run_native(args):
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        v, cores, desc = cpu_baseline(wl, args.cpu_seconds)
+        v, cores, desc = cpu_baseline(wl, args.cpu_seconds, args.unpad)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
-    traffic = load_traffic("attn_dkdv")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(wl), "B": wl.B, "L": wl.L, "T_packed": T,
-                   "useful_pairs_per_head": pairs, "fwd_flops": fwd_flops, "bwd_flops": bwd_flops,
-                   "l2": "flushed before every step (256 MiB write, outside the timed events)",
-                   "parallelism": f"replicas x{world} (independent batches)",
-                   "attn_impl": args.attn_impl},
-        "roofline": {"kernel": "attn_dkdv_tc_kernel (split-attention backward, dK and dV)",
-                     "bound": "tensor", "achieved": dkdv_tflops, "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": dkdv_tflops / peaks["bf16_tflops"],
-                     "traffic": traffic, "flops_per_launch": dkdv_flops, "launch_ms": dkdv_ms,
-                     "peak_source": f"{peaks['source']} bf16 dense burst (MEASURED_PEAKS.json)"},
+        "config": {"workload": workload_desc(wl, args.unpad), "B": wl.B, "L": wl.L, "T_packed": T_main,
+                   "useful_pairs_per_head": summ["useful_pairs_per_head"], "fwd_flops": 4.0 * wl.D * wl.Hq * summ["useful_pairs_per_head"],
+                   "bwd_flops": (10.0 if wl.backward else 0.0) * wl.D * wl.Hq * summ["useful_pairs_per_head"],
+                   "l2": "flushed before every step (256 MiB write, outside the timed events); inputs exceed L2",
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "tokens_per_s": summ["unique_tokens_per_s"],
+        "tokens_per_s_note": "unique (packed) tokens per second over the whole step; batch_tokens_per_s counts B*L",
+        "batch_tokens_per_s": summ["batch_tokens_per_s"],
+        "frac_of_sustained_peak": value / (world * peaks["bf16_tflops_sustained"]),
+        "frac_of_burst_peak": value / (world * peaks["bf16_tflops"]),
+        "roofline": {"kernel": KERNEL_NAMES[dom], "bound": "tensor", "achieved": dom_tflops,
+                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": dom_tflops / peaks["bf16_tflops_sustained"],
+                     "frac_of_burst": dom_tflops / peaks["bf16_tflops"],
+                     "traffic": traffic, "traffic_source": traffic_src,
+                     "flops_per_launch": dom_flops, "launch_ms": dom_ms,
+                     "peak_source": f"{peaks['source']} bf16 dense, sustained (MEASURED_PEAKS.json): the kernel "
+                                    f"runs inside a seconds-long loop of steps"},
         "kernels": kernel_ms,
+        "kernel_tflops": kernel_tflops,
         "breakdown_ms": med,
-        "attn_fwd": {"tflops": fwd_tflops, "frac_of_measured_peak": fwd_tflops / peaks["bf16_tflops"]},
-        "attn_bwd": {"tflops": bwd_tflops, "frac_of_measured_peak": bwd_tflops / peaks["bf16_tflops"]},
-        "pack": {"kernel": "pack_rows of the [B, L, 1024] bf16 hidden states", "bytes": pack_bytes,
-                 "gbs": pack_gbs, "frac_of_measured_hbm": pack_gbs / peaks["hbm_gbs"],
+        "attn_fwd": {"tflops": summ["attn_fwd_tflops"],
+                     "frac_of_sustained_peak": summ["attn_fwd_tflops"] / peaks["bf16_tflops_sustained"]},
+        "attn_bwd": None if not wl.backward else {
+            "tflops": summ["attn_bwd_tflops"],
+            "frac_of_sustained_peak": summ["attn_bwd_tflops"] / peaks["bf16_tflops_sustained"]},
+        "pack": {"kernel": "pack_rows of the [B, L, 1024] bf16 hidden states", **summ["pack_hidden"],
                  "ids_positions_ms": med["pack"]},
         "reconstruct": {"kernel": "reconstruct of the attention output [T, Hq*D] bf16 to [B, L, Hq*D]",
-                        "bytes": recon_bytes, "gbs": recon_gbs,
-                        "frac_of_measured_hbm": recon_gbs / peaks["hbm_gbs"]},
+                        **summ["reconstruct"]},
         "reconstruct_backward": {"kernel": "adjoint of the reconstruction, [B, L, Hq*D] bf16 gradient to [T, Hq*D] "
                                            "(shared prompt rows summed over members); timed apart from the step",
                                  "bytes": rb_bytes, "ms": rb_ms, "gbs": rb_gbs,
                                  "frac_of_measured_hbm": rb_gbs / peaks["hbm_gbs"]},
         "standard_attention": std,
+        "workloads": extras,
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clock_info,

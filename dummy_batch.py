@@ -65,6 +65,10 @@ WORKLOADS = {
     # the same with 64 distinct prompts (nothing to deduplicate)
     "pipeline_nodedup": Workload("pipeline_nodedup", 64, 1, 4096, 1024, 151936, 16, 8, 128,
                                  "bf16", True, resp_len_range=(256, 1024), hidden=1024),
+    # one group of the long-context workload (1 prompt of 32768 x 8 responses
+    # of 2048): the same kernels and tiles on a quarter of the data, the size
+    # used for single-kernel profiler captures
+    "long_context_1g": Workload("long_context_1g", 1, 8, 32768, 2048, 151936, 16, 8, 128, "bf16", True),
 }
 
 SEED_BASE = 1000

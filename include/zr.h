@@ -16,11 +16,14 @@
  *    asynchronous on that stream; the only host synchronisations are the
  *    optional host read-backs named in a call (num_groups_host, T_host) and
  *    zr_check_status.
- *  - Arguments are validated on the host before any launch.  A call that
- *    returns anything but ZR_OK has launched nothing.  Kernel launch errors are
- *    ZR_ERR_CUDA.  Conditions that only the device can see (an unsupported mask
- *    layout, a packed capacity that is too small, a bounded wait that ran out)
- *    are written to the device status words of the reconstruction info and
+ *  - Arguments are validated on the host before any launch: a call that
+ *    returns ZR_ERR_INVALID_ARG, ZR_ERR_UNSUPPORTED or ZR_ERR_WORKSPACE has
+ *    launched nothing.  The one status found after launching is the
+ *    ZR_ERR_CAPACITY of zr_pack_dedup with a host read-back (its plan kernel
+ *    has run; nothing was gathered).  Kernel launch errors are ZR_ERR_CUDA.
+ *    Conditions that only the device can see (an unsupported mask layout, a
+ *    packed capacity that is too small, a bounded wait that ran out) are
+ *    written to the device status words of the reconstruction info and
  *    reported by zr_check_status.
  *  - No C++ exception crosses this interface.
  *  - The row tensors are token-major and contiguous:
@@ -63,9 +66,6 @@ int zr_version(void);
 int64_t zr_kernel_launches(void);
 
 /* Test and tuning knobs (process-wide, not thread-safe; set before use):
- *  "attn_impl"   0 = automatic, 1 = SIMT kernels, 2 = tensor-core kernels
- *                (ZR_ERR_UNSUPPORTED from the attention calls when the shape
- *                has no tensor-core kernel)
  *  "weak_hash"   1 = every prompt hashes to the same value (forces the exact
  *                row comparison to resolve all groups; results are unchanged)
  *  "wait_limit"  bounded-wait limit of the tensor-core kernels in polls
@@ -141,7 +141,10 @@ zr_status zr_find_prompt_groups(const int64_t* input_ids, const uint8_t* attenti
  * workspace.  Limit: B <= 4096 rows (larger B returns ZR_ERR_UNSUPPORTED
  * before any launch).  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  Every call on a device shares the
+ * first call before any stream capture.  The address is cached per device
+ * together with the ID of the CUDA context it belongs to: after a
+ * cudaDeviceReset the next call on that device sees a new context and repeats
+ * the look-up, so that call, too, belongs before any stream capture.  Every call on a device shares the
  * one array, which keeps the previous call's contents (the call clears what
  * must start at zero): calls that can overlap on the GPU -- on different
  * streams, or from different host threads -- race and must be serialised by
@@ -304,9 +307,11 @@ zr_status zr_batch_stats_compute(const uint8_t* attention_mask, int B, int L, in
  * response rows up to itself.  Pad rows (mask 0) are never attended; their
  * outputs, LSE and gradients are written as zero.
  *
- *  dtype         ZR_BF16 (bf16 in/out, fp32 accumulation) or ZR_F32
- *  D             head dimension: 64 or 128 for bf16 tensor-core kernels;
- *                any multiple of 32 up to 256 for the SIMT kernels
+ *  dtype         ZR_BF16: bf16 in/out with fp32 accumulation, on the
+ *                tensor-core kernels (every GQA ratio, MHA included);
+ *                ZR_F32: float32 in/out, on the SIMT (CUDA-core) kernels
+ *  D             head dimension: 64 or 128 for ZR_BF16; 32, 64, 96 or 128
+ *                for ZR_F32 (other values: ZR_ERR_UNSUPPORTED)
  *  softmax_scale <= 0 selects 1/sqrt(D)
  *  workspace     zr_split_attn_workspace(info, Hq, Hkv, D) bytes, 256-aligned
  * The backward takes o and lse from the forward and recomputes the attention

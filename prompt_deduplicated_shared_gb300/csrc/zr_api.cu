@@ -130,10 +130,7 @@ int64_t zr_kernel_launches(void) { return g_launches.load(std::memory_order_rela
 
 zr_status zr_set_option(const char* name, int64_t value) {
     if (!name) return set_error(ZR_ERR_INVALID_ARG, "option name is NULL");
-    if (!strcmp(name, "attn_impl")) {
-        if (value < 0 || value > 2) return set_error(ZR_ERR_INVALID_ARG, "attn_impl must be 0, 1 or 2");
-        options().attn_impl = (int)value;
-    } else if (!strcmp(name, "weak_hash")) {
+    if (!strcmp(name, "weak_hash")) {
         options().weak_hash = value != 0;
     } else if (!strcmp(name, "wait_limit")) {
         if (value < 0) return set_error(ZR_ERR_INVALID_ARG, "wait_limit must be >= 0");
@@ -374,8 +371,10 @@ static zr_status attn_common(const zr_recon_info* info, int Hq, int Hkv, int D, 
     if (Hq <= 0 || Hkv <= 0) return set_error(ZR_ERR_INVALID_ARG, "Hq=%d Hkv=%d must be positive", Hq, Hkv);
     if (Hq % Hkv) return set_error(ZR_ERR_UNSUPPORTED, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
     if (dtype != ZR_BF16 && dtype != ZR_F32) return set_error(ZR_ERR_UNSUPPORTED, "dtype %d", (int)dtype);
-    if (D != 32 && D != 64 && D != 96 && D != 128)
-        return set_error(ZR_ERR_UNSUPPORTED, "head_dim %d (supported: 32, 64, 96, 128)", D);
+    if (dtype == ZR_BF16 && D != 64 && D != 128)
+        return set_error(ZR_ERR_UNSUPPORTED, "bf16 head_dim %d (the tensor-core kernels take 64 or 128)", D);
+    if (dtype == ZR_F32 && D != 32 && D != 64 && D != 96 && D != 128)
+        return set_error(ZR_ERR_UNSUPPORTED, "float32 head_dim %d (supported: 32, 64, 96, 128)", D);
     const size_t need = attn_workspace_layout(*info, Hq, D, nullptr, nullptr);
     if (!workspace || workspace_bytes < need || !aligned256(workspace))
         return set_error(ZR_ERR_WORKSPACE, "attention workspace needs %zu bytes, 256-aligned", need);
@@ -396,16 +395,16 @@ zr_status zr_split_attn_fwd(const zr_recon_info* info, const void* q, const void
     a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.dtype = dtype;
     a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
     a.T_cap = info->T_cap;
-    const int impl = options().attn_impl;
-    const bool tc_ok = tc_fwd_supported(a);
-    if (impl == 2 && !tc_ok)
-        return set_error(ZR_ERR_UNSUPPORTED, "no tensor-core forward for dtype=%d D=%d Hq/Hkv=%d",
-                         (int)dtype, D, Hq / Hkv);
+    // bf16 runs on the tensor cores, float32 on the SIMT kernels (attn_common
+    // has rejected every other shape)
+    const bool tc = dtype == ZR_BF16;
+    if (tc && !tc_fwd_supported(a))
+        return set_error(ZR_ERR_UNSUPPORTED, "no tensor-core forward for D=%d Hq=%d Hkv=%d", D, Hq, Hkv);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ZR_CUDA_TRY(cudaMemsetAsync(ws.status, 0, 4 * sizeof(int), s));
     st = launch_attn_plan(*info, ws, s);
     if (st != ZR_OK) return st;
-    st = (impl != 1 && tc_ok) ? launch_attn_fwd_tc(*info, ws, a, s) : launch_attn_fwd_simt(*info, ws, a, s);
+    st = tc ? launch_attn_fwd_tc(*info, ws, a, s) : launch_attn_fwd_simt(*info, ws, a, s);
     if (st != ZR_OK) return st;
     const int64_t e = dtype == ZR_F32 ? 4 : 2;
     st = launch_zero_pad_rows(*info, o, (int64_t)Hq * D * e, s);
@@ -428,16 +427,14 @@ zr_status zr_split_attn_bwd(const zr_recon_info* info, const void* q, const void
     a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.dtype = dtype;
     a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
     a.T_cap = info->T_cap;
-    const int impl = options().attn_impl;
-    const bool tc_ok = tc_bwd_supported(a);
-    if (impl == 2 && !tc_ok)
-        return set_error(ZR_ERR_UNSUPPORTED, "no tensor-core backward for dtype=%d D=%d Hq/Hkv=%d",
-                         (int)dtype, D, Hq / Hkv);
+    const bool tc = dtype == ZR_BF16;
+    if (tc && !tc_bwd_supported(a))
+        return set_error(ZR_ERR_UNSUPPORTED, "no tensor-core backward for D=%d Hq=%d Hkv=%d", D, Hq, Hkv);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ZR_CUDA_TRY(cudaMemsetAsync(ws.status, 0, 4 * sizeof(int), s));
     st = launch_attn_plan(*info, ws, s);
     if (st != ZR_OK) return st;
-    if (impl != 1 && tc_ok) {
+    if (tc) {
         st = launch_attn_bwd_tc(*info, ws, a, s);  // computes its own head-major Delta
     } else {
         st = launch_attn_delta(*info, ws, a, s);
@@ -470,6 +467,8 @@ zr_status zr_check_status(const zr_recon_info* info, void* attn_workspace, void*
         return set_error(ZR_ERR_INVALID_ARG, "attention_mask layout unsupported: prompts must be "
                          "left padded and responses right padded");
     if (hs[kStatusCapacity]) return set_error(ZR_ERR_CAPACITY, "packed tokens exceed T_cap");
+    if (hs[kStatusTimeout])
+        return set_error(ZR_ERR_TIMEOUT, "a bounded device wait gave up (code %d)", hs[kStatusTimeout]);
     if (ha[kStatusTimeout])
         return set_error(ZR_ERR_TIMEOUT, "a bounded device wait gave up (code %d)", ha[kStatusTimeout]);
     return ZR_OK;

@@ -1,8 +1,8 @@
 // Split attention on CUDA cores (SIMT), forward and backward.
 //
-// This is the exact-fp32 path (float32 inputs, e.g. the 2-head, head_dim 64
-// parity configuration) and the path for bf16 shapes without a tensor-core
-// kernel.  It computes the same split attention as the tensor-core kernels
+// This is the float32 path (float32 inputs and outputs, e.g. the 2-head,
+// head_dim 64 parity configuration); bf16 attention runs only on the
+// tensor-core kernels.  It computes the same split attention as those kernels
 // ("How Prompt Deduplication Works", "Split Attention Optimization") from the
 // same tile lists: a query tile of 128 rows attends the group's valid prompt
 // [pk0, pk1) and the causal range [ck0, row].
@@ -11,7 +11,6 @@
 // dimension (DPL = D/32 values per lane); a block of 16 warps owns a 128-row
 // tile and stages 32 keys (or queries) at a time in shared memory as fp32.
 // Softmax runs in base 2 with the scale folded into log2(e).
-#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -29,14 +28,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
-template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
-    return __bfloat162float(x);
-}
 template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
-template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
-    return __float2bfloat16_rn(x);
-}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -414,30 +407,26 @@ zr_status bwd_by_dim(const zr_recon_info& info, const AttnWorkspace& ws, const A
 
 zr_status launch_attn_fwd_simt(const zr_recon_info& /*info*/, const AttnWorkspace& ws,
                                const AttnArgs& a, cudaStream_t s) {
-    if (a.dtype == ZR_F32) return fwd_by_dim<float>(ws, a, s);
-    return fwd_by_dim<__nv_bfloat16>(ws, a, s);
+    if (a.dtype != ZR_F32) return set_error(ZR_ERR_UNSUPPORTED, "SIMT attention is float32 only");
+    return fwd_by_dim<float>(ws, a, s);
 }
 
 zr_status launch_attn_delta(const zr_recon_info& info, const AttnWorkspace& ws, const AttnArgs& a,
                             cudaStream_t s) {
     const int64_t warps = a.T_cap * a.Hq;
     const int64_t blocks = (warps * 32 + 255) / 256;
-    if (a.dtype == ZR_F32)
-        attn_delta_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
-            static_cast<const float*>(a.o_in), static_cast<const float*>(a.dout), info.total_tokens,
-            a.T_cap, a.Hq, a.D, ws.delta);
-    else
-        attn_delta_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(a.o_in), static_cast<const __nv_bfloat16*>(a.dout),
-            info.total_tokens, a.T_cap, a.Hq, a.D, ws.delta);
+    if (a.dtype != ZR_F32) return set_error(ZR_ERR_UNSUPPORTED, "SIMT attention is float32 only");
+    attn_delta_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
+        static_cast<const float*>(a.o_in), static_cast<const float*>(a.dout), info.total_tokens,
+        a.T_cap, a.Hq, a.D, ws.delta);
     ZR_LAUNCH_CHECK("attn_delta_kernel");
     return ZR_OK;
 }
 
 zr_status launch_attn_bwd_simt(const zr_recon_info& info, const AttnWorkspace& ws,
                                const AttnArgs& a, cudaStream_t s) {
-    if (a.dtype == ZR_F32) return bwd_by_dim<float>(info, ws, a, s);
-    return bwd_by_dim<__nv_bfloat16>(info, ws, a, s);
+    if (a.dtype != ZR_F32) return set_error(ZR_ERR_UNSUPPORTED, "SIMT attention is float32 only");
+    return bwd_by_dim<float>(info, ws, a, s);
 }
 
 }  // namespace zr

@@ -7,13 +7,18 @@
 // The tile lists come from zr_attn_plan.cu.
 //
 // One persistent CTA per SM processes work units (query tile, pair of query
-// heads that share one key/value head).  The two heads of a pair are two
-// 128-row query tiles that see exactly the same keys, so every K/V block is
-// loaded once by TMA and used by both ("GQA packing").
+// heads 2p and 2p + 1).  The two heads of a pair are two 128-row query tiles
+// that see exactly the same key positions.  When both heads read the same
+// key/value head (an even GQA ratio) every K/V block is loaded once by TMA
+// and used by both ("GQA packing"); otherwise (odd ratios, MHA) each head
+// slot streams the blocks of its own key/value head.  With an odd number of
+// query heads the last pair is (Hq - 1, Hq - 1): slot 1 repeats slot 0's head
+// and stores nothing.
 //
 // Warp roles (576 threads):
 //   warp 0      TMA producer: Q tiles, then the K/V blocks of each unit in
-//               the order the MMAs consume them (K_0, K_1, V_0, K_2, V_1, ...)
+//               the order the MMAs consume them (shared: K_0, K_1, V_0, K_2,
+//               V_1, ...; per slot: K0_0, K1_0, K0_1, V0_0, K1_1, V1_0, ...)
 //               through an NS-slot ring
 //   warp 1      MMA issuer for both heads, in pipe order: S_t = Q_t K_j^T into
 //               TMEM, then, once the softmax has written P_t(j) back into the
@@ -62,8 +67,8 @@ struct FwdCfg {
     static constexpr int kQBytes = 128 * D * 2;
     static constexpr int kKVBytes = 128 * D * 2;
     static constexpr int kStages = D == 128 ? 4 : 8;
-    // qfull, qempty, kvfull[S], kvempty[S], sfull[2], pfull[2], odone[2], xchg[2], unit ring (4)
-    static constexpr int kNumBars = 2 + 2 * kStages + 8 + 4;
+    // qfull, qempty, kvfull[S], kvempty[S], sfull[2], pfull[2], odone[2], xchg[2], unit ring (4), mma drain
+    static constexpr int kNumBars = 2 + 2 * kStages + 8 + 4 + 1;
     // row-max exchange [2 parities][2 heads][2 parts][128] and row-sum exchange [2][2][128]
     static constexpr int kXFloats = 2 * 2 * 2 * 128 + 2 * 2 * 128;
     static constexpr int kDataBytes = 2 * kQBytes + kStages * kKVBytes;
@@ -78,7 +83,7 @@ struct FwdParams {
     const int* counts;
     const int* group_off;
     int B;
-    int npairs;       // query-head pairs
+    int npairs;       // query-head pairs, (Hq + 1) / 2
     int ratio;        // Hq / Hkv
     int Hq;
     __nv_bfloat16* o;
@@ -88,6 +93,35 @@ struct FwdParams {
     int* sched;       // global unit counter (zeroed by the plan kernel)
     long long limit;
 };
+
+// Query heads of pair hp (slot 1 repeats the last head when Hq is odd) and
+// whether the two slots read different key/value heads.
+struct PairHeads {
+    int h[2];
+    int hk[2];
+    bool split;
+};
+__device__ __forceinline__ PairHeads pair_heads(int hp, int Hq, int ratio) {
+    PairHeads r;
+    r.h[0] = 2 * hp;
+    r.h[1] = min(2 * hp + 1, Hq - 1);
+    r.hk[0] = r.h[0] / ratio;
+    r.hk[1] = r.h[1] / ratio;
+    r.split = r.hk[0] != r.hk[1];
+    return r;
+}
+
+// Ring position (relative to the unit's first load) of the K/V loads of one
+// unit with n key blocks.  W = 1 when the slots share their K/V, else 2 and
+// slot t's loads follow slot (t - 1)'s.  Block 0: K_t(0) at t.  Block j in
+// [1, n): K_t(j) at W + 2W(j - 1) + 2t and V_t(j - 1) right after it.  Last:
+// V_t(n - 1) at W + 2W(n - 1) + t.  A unit takes 2Wn positions.
+__device__ __forceinline__ int pos_k(int W, int j, int t) {
+    return j == 0 ? t : W + 2 * W * (j - 1) + 2 * t;
+}
+__device__ __forceinline__ int pos_v(int W, int n, int j, int t) {
+    return j == n - 1 ? W + 2 * W * (n - 1) + t : W + 2 * W * j + 2 * t + 1;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -114,9 +148,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8);
     const UnitRing ring{b_rest + 64, b_rest + 80, reinterpret_cast<volatile int*>(misc + 16)};
+    const uint32_t b_drain = b_rest + 96;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        mbar_init(b_drain, 1);
         mbar_init(b_qfull, 1);
         mbar_init(b_qempty, 1);
         for (int s = 0; s < C::kStages; ++s) {
@@ -158,18 +194,18 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 int ti, hp;
                 decode_unit(u, p.group_off, p.B, p.npairs, ti, hp);
                 const QTile t = p.qtiles[ti];
-                const int h0 = 2 * hp, h1 = 2 * hp + 1;
-                const int hk = h0 / p.ratio;
+                const PairHeads ph = pair_heads(hp, p.Hq, p.ratio);
+                const int W = ph.split ? 2 : 1;
                 if (k > 0 && !mbar_wait(b_qempty, (k - 1) & 1, ab, 1)) { ok = false; break; }
                 mbar_expect_tx(b_qfull, 2 * C::kQBytes);
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_2d(sQ0 + c * kChunkBytes, &tm_q, h0 * D + 64 * c, t.q0, b_qfull);
-                    tma_load_2d(sQ1 + c * kChunkBytes, &tm_q, h1 * D + 64 * c, t.q0, b_qfull);
+                    tma_load_2d(sQ0 + c * kChunkBytes, &tm_q, ph.h[0] * D + 64 * c, t.q0, b_qfull);
+                    tma_load_2d(sQ1 + c * kChunkBytes, &tm_q, ph.h[1] * D + 64 * c, t.q0, b_qfull);
                 }
                 const int npb = cdiv128(t.pk1 - t.pk0);
                 const int n = t.nblk;
-                auto load = [&](const CUtensorMap* m, int row) -> bool {
+                auto load = [&](const CUtensorMap* m, int hk, int row) -> bool {
                     const int slot = kstage % C::kStages, r = kstage / C::kStages;
                     if (r > 0 && !mbar_wait(b_kvempty(slot), (r - 1) & 1, ab, 2)) return false;
                     mbar_expect_tx(b_kvfull(slot), C::kKVBytes);
@@ -180,11 +216,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     ++kstage;
                     return true;
                 };
-                if (!load(&tm_k, key_block_row(t, npb, 0))) { ok = false; break; }
-                for (int j = 0; j < n && ok; ++j) {
-                    if (j + 1 < n && !load(&tm_k, key_block_row(t, npb, j + 1))) ok = false;
-                    if (ok && !load(&tm_v, key_block_row(t, npb, j))) ok = false;
-                }
+                // the order of pos_k / pos_v
+                for (int w = 0; w < W && ok; ++w) ok = load(&tm_k, ph.hk[w], key_block_row(t, npb, 0));
+                for (int j = 1; j < n && ok; ++j)
+                    for (int w = 0; w < W && ok; ++w) {
+                        ok = load(&tm_k, ph.hk[w], key_block_row(t, npb, j));
+                        if (ok) ok = load(&tm_v, ph.hk[w], key_block_row(t, npb, j - 1));
+                    }
+                for (int w = 0; w < W && ok; ++w) ok = load(&tm_v, ph.hk[w], key_block_row(t, npb, n - 1));
+                if (!ok) break;
             }
             // drain: every load consumed and every commit landed before exit
             const long long lim = p.limit;
@@ -241,41 +281,60 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             int ti, hp;
             decode_unit(u, p.group_off, p.B, p.npairs, ti, hp);
             const int n = p.qtiles[ti].nblk;
+            const int W = pair_heads(hp, p.Hq, p.ratio).split ? 2 : 1;
             if (!wait(b_qfull, k & 1, 6)) { ok = false; break; }
             tc_fence_after();
-            // ring positions: K_0 at 0, K_j at 2j - 1, V_j at 2j + 2, V_{n-1} at 2n - 1
-            int kslot = wait_stage(base);
-            if (kslot < 0) { ok = false; break; }
-            issue_s(0, kslot);
-            issue_s(1, kslot);
-            if (leader) mma_commit(b_kvempty(kslot));
+            // ring positions from pos_k / pos_v; slot t reads the loads of w = t
+            // when the slots stream their own K/V (W = 2), else those of w = 0.
+            // A stage is released once its last reader was issued: after slot t
+            // (W = 2) or after slot 1 (W = 1).
+            for (int t = 0; t < 2 && ok; ++t) {
+                const int w = W == 2 ? t : 0;
+                int kslot = (t == 0 || W == 2) ? wait_stage(base + pos_k(W, 0, w)) : -2;
+                if (kslot == -1) { ok = false; break; }
+                if (kslot == -2) kslot = (base + pos_k(W, 0, 0)) % C::kStages;
+                issue_s(t, kslot);
+                if (leader && (W == 2 || t == 1)) mma_commit(b_kvempty(kslot));
+            }
+            if (!ok) break;
             if (n == 1 && leader) mma_commit(b_qempty);
             for (int j = 1; j < n && ok; ++j) {
-                kslot = wait_stage(base + 2 * j - 1);
-                const int vslot = kslot < 0 ? -1 : wait_stage(base + 2 * j);
-                if (vslot < 0) { ok = false; break; }
                 for (int t = 0; t < 2; ++t) {
+                    const int w = W == 2 ? t : 0;
+                    const int kst = base + pos_k(W, j, w), vst = base + pos_v(W, n, j - 1, w);
+                    int kslot, vslot;
+                    if (t == 0 || W == 2) {
+                        kslot = wait_stage(kst);
+                        vslot = kslot < 0 ? -1 : wait_stage(vst);
+                        if (vslot < 0) { ok = false; break; }
+                    } else {
+                        kslot = kst % C::kStages;
+                        vslot = vst % C::kStages;
+                    }
                     if (!issue_pv(t, vslot, j > 1)) { ok = false; break; }
                     issue_s(t, kslot);
+                    if (leader && (W == 2 || t == 1)) {
+                        mma_commit(b_kvempty(vslot));
+                        mma_commit(b_kvempty(kslot));
+                    }
                 }
                 if (!ok) break;
-                if (leader) {
-                    mma_commit(b_kvempty(vslot));
-                    mma_commit(b_kvempty(kslot));
-                    if (j == n - 1) mma_commit(b_qempty);
-                }
+                if (leader && j == n - 1) mma_commit(b_qempty);
             }
             if (!ok) break;
-            const int vslot = wait_stage(base + 2 * n - 1);
-            if (vslot < 0) { ok = false; break; }
             for (int t = 0; t < 2 && ok; ++t) {
+                const int w = W == 2 ? t : 0;
+                const int vst = base + pos_v(W, n, n - 1, w);
+                int vslot = (t == 0 || W == 2) ? wait_stage(vst) : vst % C::kStages;
+                if (vslot < 0) { ok = false; break; }
                 if (!issue_pv(t, vslot, n > 1)) { ok = false; break; }
                 if (leader) mma_commit(b_odone(t));
+                if (leader && (W == 2 || t == 1)) mma_commit(b_kvempty(vslot));
             }
             if (!ok) break;
-            if (leader) mma_commit(b_kvempty(vslot));
-            base += 2 * n;
+            base += 2 * W * n;
         }
+        drain_mmas(leader, b_drain, p.limit);
     } else {
         // ------------------------------------------------------ softmax
         const int wg = (warp - 2) >> 2;
@@ -300,7 +359,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             int ti, hp;
             decode_unit(u, p.group_off, p.B, p.npairs, ti, hp);
             const QTile tile = p.qtiles[ti];
-            const int h = 2 * hp + t;
+            const int h = pair_heads(hp, p.Hq, p.ratio).h[t];
+            // slot 1 of the last pair of an odd head count repeats slot 0's head
+            const bool own_head = t == 0 || 2 * hp + 1 < p.Hq;
             const int npb = cdiv128(tile.pk1 - tile.pk0);
             const int n = tile.nblk;
             const int row_pos = tile.q0 + r;
@@ -388,7 +449,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!xwait()) { ok = false; break; }
             const float ltot = l + xs[(1 - part) * 128 + r];
             const float inv = 1.0f / ltot;
-            const bool store = r < tile.nq;
+            const bool store = r < tile.nq && own_head;
             __nv_bfloat16* orow = p.o + ((int64_t)row_pos * p.Hq + h) * D + (D / 2) * part;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -433,13 +494,13 @@ zr_status launch_fwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     p.counts = ws.plan.counts;
     p.group_off = ws.plan.group_qtile_off;
     p.B = info.B;
-    p.npairs = a.Hq / 2;
+    p.npairs = (a.Hq + 1) / 2;
     p.ratio = a.Hq / a.Hkv;
     p.Hq = a.Hq;
     p.o = static_cast<__nv_bfloat16*>(a.o);
     p.lse = a.lse;
     p.scale_log2 = a.scale * kLog2e;
-    p.status = ws.status + kStatusTimeout;
+    p.status = info.status + kStatusTimeout;  // read by zr_check_status(info)
     p.sched = ws.plan.counts + 2;
     p.limit = wait_limit_cycles();
     ZR_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -455,8 +516,7 @@ zr_status launch_fwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
 }  // namespace
 
 bool tc_fwd_supported(const AttnArgs& a) {
-    const int ratio = a.Hkv > 0 ? a.Hq / a.Hkv : 0;
-    return a.dtype == ZR_BF16 && (a.D == 64 || a.D == 128) && ratio > 0 && ratio % 2 == 0;
+    return a.dtype == ZR_BF16 && (a.D == 64 || a.D == 128) && a.Hkv > 0 && a.Hq % a.Hkv == 0;
 }
 
 zr_status launch_attn_fwd_tc(const zr_recon_info& info, const AttnWorkspace& ws, const AttnArgs& a,

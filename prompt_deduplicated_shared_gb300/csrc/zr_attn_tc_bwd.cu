@@ -124,8 +124,8 @@ struct DqCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kTile = 128 * D * 2;  // one K or V block
     static constexpr int kStages = D == 128 ? 3 : 6;
-    // kvfull[S], kvempty[S], qd_ready, sdp_full, sdp_free, ds_full, mm_done, unit ring (4)
-    static constexpr int kNumBars = 2 * kStages + 5 + 4;
+    // kvfull[S], kvempty[S], qd_ready, sdp_full, sdp_free, ds_full, mm_done, unit ring (4), mma drain
+    static constexpr int kNumBars = 2 * kStages + 5 + 4 + 1;
     static constexpr int kDS = 128 * 128 * 2;
     static constexpr int kDataBytes = kStages * 2 * kTile + kDS;
     static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 64 + 1024;
@@ -156,9 +156,11 @@ attn_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8);
     const UnitRing ring{b_rest + 40, b_rest + 56, reinterpret_cast<volatile int*>(misc + 16)};
+    const uint32_t b_drain = b_rest + 72;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        mbar_init(b_drain, 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(b_kvfull(s), 1);
             mbar_init(b_kvempty(s), 1);
@@ -281,6 +283,7 @@ attn_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     prev_slot = slot;
                 }
             }
+            drain_mmas(leader, b_drain, p.limit);
         }
     } else if (warp >= 4) {
         // Four softmax warpgroups; warpgroup wg owns key columns [32 wg, 32 wg + 32)
@@ -433,8 +436,8 @@ struct DkvCfg {
     static constexpr int kHalfChunk = 64 * 128;
     static constexpr int kHalf = 64 * D * 2;
     static constexpr int kStages = D == 128 ? 4 : 8;  // half-slots
-    // kfull, kempty, qfull[S], qempty[S], sdp_full[2], pds_full[2], (2 unused), unit ring (4)
-    static constexpr int kNumBars = 2 + 2 * kStages + 6 + 4;
+    // kfull, kempty, qfull[S], qempty[S], sdp_full[2], pds_full[2], (2 unused), unit ring (4), mma drain
+    static constexpr int kNumBars = 2 + 2 * kStages + 6 + 4 + 1;
     static constexpr int kDataBytes = 2 * kTile + kStages * 2 * kHalf;
     // data, LSE/Delta staging (2 KB), barriers, misc words, alignment slack
     static constexpr int kSmemBytes = kDataBytes + 2048 + kNumBars * 8 + 64 + 1024;
@@ -522,9 +525,11 @@ attn_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8);
     const UnitRing ring{b_rest + 48, b_rest + 64, reinterpret_cast<volatile int*>(misc + 16)};
+    const uint32_t b_drain = b_rest + 80;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        mbar_init(b_drain, 1);
         mbar_init(b_kfull, 1);
         mbar_init(b_kempty, 1);
         for (int s = 0; s < C::kStages; ++s) {
@@ -681,6 +686,7 @@ attn_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 if (leader) mma_commit(b_qempty(prev_b));
                 if (leader) mma_commit(b_kempty);  // every MMA of the unit done: K/V reusable, dV/dK final
             }
+            drain_mmas(leader, b_drain, p.limit);
         }
     } else {
         // softmax warps: warpgroup wg owns query columns [16 wg, +16) of each
@@ -860,7 +866,7 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
     p.scale = a.scale;
     p.scale_log2 = a.scale * kLog2e;
-    p.status = ws.status + kStatusTimeout;
+    p.status = info.status + kStatusTimeout;  // read by zr_check_status(info)
     p.sched = ws.plan.counts + 3;
     p.limit = wait_limit_cycles();
     ZR_CUDA_TRY(cudaFuncSetAttribute(attn_dkdv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -15,10 +15,11 @@
 // 3. compact_groups: groups in order of their representative (first
 //    occurrence), members ascending, as CSR.
 // 4. gather_unique_prompts: unique_prompts[g] = input_ids[rep_g, 0:P].
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "zr_internal.h"
 
@@ -197,13 +198,10 @@ zr_status launch_find_groups(const int64_t* ids, const uint8_t* mask, int B, int
     match_rows_kernel<<<B, 256, 0, s>>>(ids, mask, B, L, P, hash, rep);
     ZR_LAUNCH_CHECK("match_rows_kernel");
     const size_t smem = (size_t)3 * B * sizeof(int);
-    static bool attr_set = false;
-    if (!attr_set) {
-        ZR_CUDA_TRY(cudaFuncSetAttribute(compact_groups_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         3 * kMaxGroupRows * (int)sizeof(int)));
-        attr_set = true;
-    }
+    // the attribute belongs to the current device; setting it on every call is
+    // a cheap host call and needs no per-device or cross-thread bookkeeping
+    ZR_CUDA_TRY(cudaFuncSetAttribute(compact_groups_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     3 * kMaxGroupRows * (int)sizeof(int)));
     compact_groups_kernel<<<1, 1024, smem, s>>>(rep, B, out.group_ptr, out.members, out.group_of,
                                                 out.num_groups);
     ZR_LAUNCH_CHECK("compact_groups_kernel");
@@ -236,21 +234,62 @@ constexpr size_t kNoAllocScratchBytes = ((size_t)kNoAllocMaxRows * 8 + 255) / 25
 static __device__ __align__(256) unsigned char g_group_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 256;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+
+// The cached device address of g_group_scratch, per device, together with the
+// unique ID of the CUDA context it was looked up in.  A device reset
+// (cudaDeviceReset) destroys that context and the array with it; the next
+// call sees a new context ID and looks the address up again.
+struct ScratchCache {
+    unsigned long long ctx_id = 0;
+    void* addr = nullptr;
+};
+ScratchCache g_scratch[kMaxDevices];
+std::mutex g_scratch_mu;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique ID of the calling thread's current context (0 if it cannot be read).
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // Device address of g_group_scratch on the current device.  The host-side
-// name is only a stand-in, so the address is looked up once per device (with
-// that device current) and cached.
+// name is only a stand-in, so the address is looked up with the device current
+// (cudaGetSymbolAddress), once per device and context, and cached.  When the
+// context ID cannot be read the look-up runs on every call.
 zr_status scratch_address(void** out) {
     int dev = 0;
     ZR_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return set_error(ZR_ERR_UNSUPPORTED, "device index %d", dev);
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
+    const unsigned long long id = current_context_id();
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    ScratchCache& c = g_scratch[dev];
+    if (!c.addr || id == 0 || c.ctx_id != id) {
+        void* p = nullptr;
         ZR_CUDA_TRY(cudaGetSymbolAddress(&p, g_group_scratch));
-        g_scratch_addr[dev].store(p, std::memory_order_release);
+        c.addr = p;
+        c.ctx_id = id;
     }
-    *out = p;
+    *out = c.addr;
     return ZR_OK;
 }
 

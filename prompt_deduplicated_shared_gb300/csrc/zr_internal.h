@@ -43,7 +43,6 @@ private:
 
 // process-wide options (zr_set_option)
 struct Options {
-    int attn_impl = 0;       // 0 auto, 1 simt, 2 tensor cores
     int weak_hash = 0;
     int64_t wait_limit = 0;
     int kernel_timing = 0;

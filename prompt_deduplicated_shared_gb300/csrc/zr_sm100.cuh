@@ -144,6 +144,17 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
+// Called by the whole MMA-issuing warp when it leaves its loop (normally or
+// on abort): the elected lane commits every tcgen05.mma it issued to `bar`
+// (count 1, used only here), and the warp waits, bounded, for that arrival,
+// so that no MMA is still writing TMEM when the CTA frees it.
+__device__ __forceinline__ void drain_mmas(bool leader, uint32_t bar, long long limit) {
+    __syncwarp();
+    if (leader) mma_commit(bar);
+    __syncwarp();
+    mbar_wait_drain(bar, 0, limit);
+    __syncwarp();
+}
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

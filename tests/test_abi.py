@@ -38,8 +38,10 @@ def test_version_and_options(zr):
     assert lib.zr_version() == 100
     assert lib.zr_set_option(b"no_such_option", 1) == zr.ZR_ERR_INVALID_ARG
     assert b"unknown option" in lib.zr_last_error()
-    assert lib.zr_set_option(b"attn_impl", 3) == zr.ZR_ERR_INVALID_ARG
-    assert lib.zr_set_option(b"attn_impl", 0) == zr.ZR_OK
+    # the dtype alone selects the attention kernels: there is no switch between them
+    assert lib.zr_set_option(b"attn_impl", 0) == zr.ZR_ERR_INVALID_ARG
+    assert lib.zr_set_option(b"wait_limit", -1) == zr.ZR_ERR_INVALID_ARG
+    assert lib.zr_set_option(b"wait_limit", 0) == zr.ZR_OK
 
 
 def test_kernel_time_without_records(zr):
@@ -88,6 +90,14 @@ def test_host_validation_without_launch(zr):
     assert lib.zr_split_attn_fwd(ctypes.byref(info), *args, 16, 6, 128, zr.ZR_BF16, 0.0,
                                  ctypes.c_void_p(1 << 20), ws_bytes, None) == zr.ZR_ERR_UNSUPPORTED
     assert lib.zr_split_attn_fwd(ctypes.byref(info), *args, 16, 8, 80, zr.ZR_BF16, 0.0,
+                                 ctypes.c_void_p(1 << 20), ws_bytes, None) == zr.ZR_ERR_UNSUPPORTED
+    # bf16 head dims without a tensor-core kernel are refused, not run elsewhere
+    for D in (32, 96):
+        ws_d = lib.zr_split_attn_workspace(ctypes.byref(info), 16, 8, D)
+        assert lib.zr_split_attn_fwd(ctypes.byref(info), *args, 16, 8, D, zr.ZR_BF16, 0.0,
+                                     ctypes.c_void_p(1 << 20), ws_d, None) == zr.ZR_ERR_UNSUPPORTED
+        assert b"tensor-core" in lib.zr_last_error()
+    assert lib.zr_split_attn_fwd(ctypes.byref(info), *args, 16, 8, 256, zr.ZR_F32, 0.0,
                                  ctypes.c_void_p(1 << 20), ws_bytes, None) == zr.ZR_ERR_UNSUPPORTED
     assert lib.zr_split_attn_fwd(ctypes.byref(info), *args, 16, 8, 128, zr.ZR_BF16, 0.0,
                                  ctypes.c_void_p(1 << 20), ws_bytes - 1, None) == zr.ZR_ERR_WORKSPACE

@@ -25,33 +25,30 @@ def zr():
     return lib()
 
 
-def _impls(zr, dtype, D, ratio):
-    impls = [1]
-    if dtype == torch.bfloat16 and D in (64, 128):
-        impls.append(2)
-    return impls
+def _tc_expected(dtype, D):
+    """bf16 attention runs on the tensor-core kernels for every GQA ratio
+    (head_dim 64 or 128); float32 runs on the SIMT kernels."""
+    return dtype == torch.bfloat16 and D in (64, 128)
 
 
-def _run(zr, impl, info, tq, tk, tv, tdo, backward=True):
-    zr.set_option("attn_impl", impl)
+def _run(zr, info, tq, tk, tv, tdo, backward=True):
+    """Forward (and backward) through the C ABI; any error status fails the
+    test.  The per-kernel event records show which kernels ran: the
+    tensor-core forward and backward for bf16, none of them for float32."""
+    zr.kernel_time_reset()
+    zr.set_option("kernel_timing", 1)
     try:
-        try:
-            o, lse = zr.split_attn_fwd(info, tq, tk, tv)
-        except zr.ZrError as e:
-            if e.status == zr.ZR_ERR_UNSUPPORTED and impl == 2:
-                return None  # no tensor-core kernel for this shape
-            raise
-        grads = None
-        if backward:
-            try:
-                grads = zr.split_attn_bwd(info, tq, tk, tv, o, lse, tdo)
-            except zr.ZrError as e:
-                if not (e.status == zr.ZR_ERR_UNSUPPORTED and impl == 2):
-                    raise
+        o, lse = zr.split_attn_fwd(info, tq, tk, tv)
+        grads = zr.split_attn_bwd(info, tq, tk, tv, o, lse, tdo) if backward else None
         torch.cuda.synchronize()
         zr.check_status(info)
+        launched = {n: zr.kernel_time(n)[1] for n in ("attn_fwd", "attn_dkdv")}
     finally:
-        zr.set_option("attn_impl", 0)
+        zr.set_option("kernel_timing", 0)
+        zr.kernel_time_reset()
+    tc = _tc_expected(tq.dtype, tq.shape[2])
+    assert launched["attn_fwd"] == (1 if tc else 0), launched
+    assert launched["attn_dkdv"] == (1 if tc and backward else 0), launched
     return o, lse, grads
 
 
@@ -61,6 +58,10 @@ DENSE = [
     ("fp32-ragged", 2, 3, 150, 70, 4, 2, 32, torch.float32, (1, 70), None, False),
     ("bf16-d128", 2, 3, 300, 140, 4, 2, 128, torch.bfloat16, None, None, False),
     ("bf16-d64-mha", 3, 2, 129, 257, 2, 2, 64, torch.bfloat16, (1, 257), None, False),
+    ("bf16-d128-mha", 2, 2, 200, 130, 4, 4, 128, torch.bfloat16, (5, 130), None, False),
+    ("bf16-d128-ratio3", 2, 2, 250, 100, 6, 2, 128, torch.bfloat16, (1, 100), None, False),
+    ("bf16-d64-odd-heads", 2, 2, 140, 90, 5, 5, 64, torch.bfloat16, (1, 90), None, False),
+    ("bf16-d128-ratio3-odd", 1, 3, 170, 60, 3, 1, 128, torch.bfloat16, (1, 60), None, False),
     ("bf16-unpad", 2, 4, 200, 100, 4, 2, 128, torch.bfloat16, (3, 100), None, True),
     ("bf16-leftpad", 2, 2, 190, 60, 4, 1, 128, torch.bfloat16, (1, 60), (1, 70), False),
     ("bf16-leftpad-unpad", 2, 2, 190, 60, 8, 2, 64, torch.bfloat16, (1, 60), (1, 70), True),
@@ -80,20 +81,13 @@ def test_dense_parity(zr, case):
     (q, k, v, do), (tq, tk, tv, tdo) = qkv_inputs(T, Hq, Hkv, D, 5, dtype)
     o_ref, lse_ref = oracle.split_attention_fwd(q, k, v, info_ref)
     dq_ref, dk_ref, dv_ref = oracle.split_attention_bwd(q, k, v, do, info_ref)
-    for impl in _impls(zr, dtype, D, Hq // Hkv):
-        res = _run(zr, impl, info, tq, tk, tv, tdo)
-        if res is None:
-            continue
-        o, lse, grads = res
-        t = tol(dtype)
-        assert max_abs(o, o_ref) < t, (impl, "o")
-        assert max_abs(lse, lse_ref.T) < t, (impl, "lse")
-        if grads is None:
-            continue
-        dq, dk, dv = grads
-        assert max_abs(dq, dq_ref) < t, (impl, "dq")
-        assert max_abs(dk, dk_ref) < t, (impl, "dk")
-        assert max_abs(dv, dv_ref) < t, (impl, "dv")
+    o, lse, (dq, dk, dv) = _run(zr, info, tq, tk, tv, tdo)
+    t = tol(dtype)
+    assert max_abs(o, o_ref) < t, "o"
+    assert max_abs(lse, lse_ref.T) < t, "lse"
+    assert max_abs(dq, dq_ref) < t, "dq"
+    assert max_abs(dk, dk_ref) < t, "dk"
+    assert max_abs(dv, dv_ref) < t, "dv"
 
 
 def test_reduced_qwen_structure(zr):
@@ -105,19 +99,12 @@ def test_reduced_qwen_structure(zr):
     (q, k, v, do), (tq, tk, tv, tdo) = qkv_inputs(T, 16, 8, 128, 22, torch.bfloat16)
     o_ref, lse_ref = oracle.split_attention_fwd(q, k, v, info_ref)
     dq_ref, dk_ref, dv_ref = oracle.split_attention_bwd(q, k, v, do, info_ref)
-    for impl in _impls(zr, torch.bfloat16, 128, 2):
-        res = _run(zr, impl, info, tq, tk, tv, tdo)
-        if res is None:
-            continue
-        o, lse, grads = res
-        assert max_abs(o, o_ref) < 2e-2
-        assert max_abs(lse, lse_ref.T) < 2e-2
-        if grads is None:
-            continue
-        dq, dk, dv = grads
-        assert max_abs(dq, dq_ref) < 2e-2
-        assert max_abs(dk, dk_ref) < 2e-2
-        assert max_abs(dv, dv_ref) < 2e-2
+    o, lse, (dq, dk, dv) = _run(zr, info, tq, tk, tv, tdo)
+    assert max_abs(o, o_ref) < 2e-2
+    assert max_abs(lse, lse_ref.T) < 2e-2
+    assert max_abs(dq, dq_ref) < 2e-2
+    assert max_abs(dk, dk_ref) < 2e-2
+    assert max_abs(dv, dv_ref) < 2e-2
 
 
 def _sample_rows(info, per_segment, rng):
@@ -133,41 +120,44 @@ def _sample_rows(info, per_segment, rng):
     return sorted(set(t for t in rows if info.row_valid[t]))
 
 
-@pytest.mark.parametrize("wname", ["qwen3_0p6b", "worked_example", "pipeline", "long_context"])
-def test_full_size_sampled(zr, wname):
+FULL = [("qwen3_0p6b", False), ("worked_example", False), ("pipeline", False), ("pipeline", True),
+        ("pipeline_nodedup", False), ("long_context", False)]
+
+
+@pytest.mark.parametrize("wname,use_unpad", FULL, ids=[f"{w}-{'unpad' if u else 'pad'}" for w, u in FULL])
+def test_full_size_sampled(zr, wname, use_unpad):
+    """Every configuration at full size, in the launch configuration the bench
+    uses: the forward on sampled query rows of every prompt and response, the
+    backward with the upstream gradient zero outside a sampled row set (the
+    exact gradients then need one row of attention per sampled row)."""
     wl = WORKLOADS[wname]
     idx = list(WORKLOADS).index(wname)
     ids, mask, pos = make_workload_batch(wl, idx)
-    _, _, _, _, info_ref = oracle_pack(ids, mask, pos, wl.R, False)
-    _, _, _, _, info, T = gpu_pack(zr, ids, mask, pos, wl.R, False, T_cap=info_ref.T)
+    _, _, _, _, info_ref = oracle_pack(ids, mask, pos, wl.R, use_unpad)
+    _, _, _, _, info, T = gpu_pack(zr, ids, mask, pos, wl.R, use_unpad, T_cap=info_ref.T)
+    assert T == info_ref.T
     (q, k, v, do), (tq, tk, tv, tdo) = qkv_inputs(T, wl.Hq, wl.Hkv, wl.D, 100 + idx, torch.bfloat16)
-    rng = np.random.default_rng(idx)
-    per = 2 if wname == "long_context" else 6
+    rng = np.random.default_rng(idx + (50 if use_unpad else 0))
+    per = 2 if wname in ("long_context", "pipeline_nodedup") else 6
     rows = _sample_rows(info_ref, per, rng)
     keysets = oracle.row_key_sets(info_ref)
     o_ref, lse_ref = oracle.split_attention_fwd_rows(q, k, v, info_ref, rows, key_sets=keysets)
     sparse_do = np.zeros_like(do)
-    bwd_rows = rows[::3] if wname == "long_context" else rows
+    bwd_rows = rows[::3] if wname in ("long_context", "pipeline_nodedup") else rows
     sparse_do[bwd_rows] = do[bwd_rows]
     tdo_sparse = torch.from_numpy(sparse_do).to(DEV, torch.bfloat16)
     want_bwd = wl.backward
     if want_bwd:
         dq_ref, dk_ref, dv_ref = oracle.split_attention_bwd_sparse(q, k, v, sparse_do, info_ref,
                                                                    bwd_rows, key_sets=keysets)
-    for impl in _impls(zr, torch.bfloat16, wl.D, wl.Hq // wl.Hkv):
-        if impl == 1 and wname == "long_context":
-            continue  # the SIMT path at this size takes minutes
-        res = _run(zr, impl, info, tq, tk, tv, tdo_sparse, backward=want_bwd)
-        if res is None:
-            continue
-        o, lse, grads = res
-        assert max_abs(o[rows], o_ref) < 2e-2, (impl, "o")
-        assert max_abs(lse[rows], lse_ref.T) < 2e-2, (impl, "lse")
-        if want_bwd and grads is not None:
-            dq, dk, dv = grads
-            assert max_abs(dq, dq_ref) < 2e-2, (impl, "dq")
-            assert max_abs(dk, dk_ref) < 2e-2, (impl, "dk")
-            assert max_abs(dv, dv_ref) < 2e-2, (impl, "dv")
+    o, lse, grads = _run(zr, info, tq, tk, tv, tdo_sparse, backward=want_bwd)
+    assert max_abs(o[rows], o_ref) < 2e-2, "o"
+    assert max_abs(lse[rows], lse_ref.T) < 2e-2, "lse"
+    if want_bwd:
+        dq, dk, dv = grads
+        assert max_abs(dq, dq_ref) < 2e-2, "dq"
+        assert max_abs(dk, dk_ref) < 2e-2, "dk"
+        assert max_abs(dv, dv_ref) < 2e-2, "dv"
 
 
 def test_kernel_timing_counts_launches_and_changes_nothing(zr):
@@ -177,11 +167,19 @@ def test_kernel_timing_counts_launches_and_changes_nothing(zr):
     _, _, _, _, info_ref = oracle_pack(ids, mask, pos, 140, False)
     _, _, _, _, info, T = gpu_pack(zr, ids, mask, pos, 140, False, T_cap=info_ref.T)
     _, (tq, tk, tv, tdo) = qkv_inputs(T, 4, 2, 128, 6, torch.bfloat16)
-    plain = _run(zr, 2, info, tq, tk, tv, tdo)
+
+    def plain_run():
+        o, lse = zr.split_attn_fwd(info, tq, tk, tv)
+        grads = zr.split_attn_bwd(info, tq, tk, tv, o, lse, tdo)
+        torch.cuda.synchronize()
+        zr.check_status(info)
+        return o, lse, grads
+
+    plain = plain_run()
     zr.kernel_time_reset()
     zr.set_option("kernel_timing", 1)
     try:
-        timed = _run(zr, 2, info, tq, tk, tv, tdo)
+        timed = plain_run()
         times = {n: zr.kernel_time(n) for n in ("attn_fwd", "attn_bwd_prep", "attn_dkdv", "attn_dq")}
     finally:
         zr.set_option("kernel_timing", 0)
@@ -241,3 +239,40 @@ def test_standard_qkv_path_equals_split_attention(zr):
         ref = zr.reconstruct_backward(info, full.float().view(B, L, -1))[:T]
         d = (got.float().view(T, -1) - ref).abs() - 2 * 2.0 ** -8 * ref.abs()
         assert float(d.max()) < tol, name
+
+
+def test_standard_strategy_against_oracle(zr):
+    """The standard strategy ("Split Attention Optimization", split attention
+    off: Q, K, V reconstructed to the full batch, then ordinary causal
+    attention) against the oracle, element by element.  Q, K, V and dO are
+    drawn on the deduplicated packed rows and reconstructed to [B, L] rows on
+    both sides (the GPU reconstruction is bit-exact against the oracle's, see
+    test_gpu_dedup); the GPU then runs its kernels over the identity grouping,
+    and the oracle runs its duplicated per-sequence causal attention with
+    every row its own group."""
+    G, n, P, R, Hq, Hkv, D = 2, 3, 300, 140, 4, 2, 128
+    ids, mask, pos = make_batch(G, n, P, R, 1000, 83, resp_len_range=(1, R))
+    B, L = ids.shape
+    _, _, _, _, info_ref = oracle_pack(ids, mask, pos, R, False)
+    _, _, _, _, info, T = gpu_pack(zr, ids, mask, pos, R, False, T_cap=info_ref.T)
+    (q, k, v, do), (tq, tk, tv, tdo) = qkv_inputs(T, Hq, Hkv, D, 15, torch.bfloat16)
+    # reconstructed full-batch tensors, [B*L, H, D]
+    qf_ref, kf_ref, vf_ref, dof_ref = (oracle.reconstruct_sequences(x.reshape(T, -1), info_ref)
+                                       .reshape(B * L, x.shape[1], D) for x in (q, k, v, do))
+    qf, kf, vf, dof = (zr.reconstruct(info, x.view(T, -1)).view(B * L, x.shape[1], D) for x in (tq, tk, tv, tdo))
+    identity = [[b] for b in range(B)]
+    _, _, info_id_ref = oracle.create_deduplicated_batch(ids, pos, R, identity, None, attention_mask=mask)
+    assert info_id_ref.T == B * L
+    o_ref, lse_ref = oracle.split_attention_fwd(qf_ref, kf_ref, vf_ref, info_id_ref)
+    dq_ref, dk_ref, dv_ref = oracle.split_attention_bwd(qf_ref, kf_ref, vf_ref, dof_ref, info_id_ref)
+    t_ids = torch.from_numpy(ids).to(DEV)
+    gi = zr.identity_groups(B, DEV)
+    _, _, _, info_id, T_id = zr.pack_dedup(t_ids, torch.from_numpy(pos).to(DEV), R, gi,
+                                           torch.from_numpy(mask).to(DEV), sync=True)
+    assert T_id == B * L
+    o, lse, (dq, dk, dv) = _run(zr, info_id, qf, kf, vf, dof)
+    assert max_abs(o, o_ref) < 2e-2, "o"
+    assert max_abs(lse, lse_ref.T) < 2e-2, "lse"
+    assert max_abs(dq, dq_ref) < 2e-2, "dq"
+    assert max_abs(dk, dk_ref) < 2e-2, "dk"
+    assert max_abs(dv, dv_ref) < 2e-2, "dv"
