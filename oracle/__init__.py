@@ -35,6 +35,7 @@ from .dedup import (  # noqa: F401
     reconstruct_sequences,
     reconstruct_backward,
     pack_rows,
+    pack_rows_backward,
     ReconstructionInfo,
 )
 from .attention import (  # noqa: F401

@@ -235,3 +235,21 @@ def reconstruct_backward(grad_out, info: ReconstructionInfo):
             _, p = info.row_src[t]
             out[t] += g[b, p]
     return out
+
+
+def pack_rows_backward(grad_packed, info: ReconstructionInfo):
+    """Adjoint of ``pack_rows`` ("Correctness & Gradients": gradients flow back
+    through the deduplication step as well as the reconstruction).  Packed row
+    t was read from source position ``row_src[t]``, so that position receives
+    ``grad_packed[t]``; every source position is read at most once, so there
+    is nothing to sum.  Positions the pack never read (the prompt rows of every
+    group member but the representative, and the pads that ``use_unpad``
+    dropped) receive zero.  Returns ``[B, L, ...]`` in the input's dtype."""
+    g = np.asarray(grad_packed)
+    if g.ndim >= 2 and g.shape[0] == 1 and g.shape[1] == info.T:
+        g = g[0]
+    out = np.zeros((info.B, info.L) + g.shape[1:], dtype=g.dtype)
+    for t, (b, p) in enumerate(info.row_src):
+        out[b, p] = g[t]
+    return out
+

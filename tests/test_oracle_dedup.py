@@ -212,6 +212,57 @@ def test_reconstruct_backward_special_cases():
     assert np.array_equal(gp[6:], np.ones(n * 3))
 
 
+@pytest.mark.parametrize("case", _ADJ_CASES)
+def test_pack_rows_backward_is_the_adjoint(case):
+    """<pack(x), y> = <x, pack_backward(y)> for random x, y (the defining
+    property of the adjoint), against the oracle's pack_rows, itself pinned by
+    reconstruct∘pack = identity and the page's packing diagram."""
+    G, n, P, R, rlr, ppr, unpad = case
+    ids, mask, pos = make_batch(G, n, P, R, 30, 19, resp_len_range=rlr, prompt_pad_range=ppr)
+    if unpad and mask is None:
+        mask = np.ones_like(ids, dtype=np.uint8)
+    groups, uniq = oracle.find_prompt_groups(ids, R, mask)
+    _, _, info = oracle.create_deduplicated_batch(ids, pos, R, groups, uniq, attention_mask=mask,
+                                                  use_unpad=unpad)
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((ids.shape[0], ids.shape[1], 3))
+    y = rng.standard_normal((info.T, 3))
+    lhs = float(np.sum(pack_rows(x, info) * y))
+    rhs = float(np.sum(x * oracle.pack_rows_backward(y, info)))
+    assert abs(lhs - rhs) <= 1e-12 * (np.abs(x).max() * np.abs(y).sum() + 1.0)
+
+
+def test_pack_rows_backward_special_cases():
+    """The pack reads every source position at most once, so its adjoint is a
+    scatter: packing a tensor and mapping it back keeps exactly the positions
+    the pack read -- the representative's whole row, and of every other member
+    only the response -- and zeroes the rest (other members' prompts, pads
+    dropped by use_unpad).  With all prompts distinct and no padding dropped it
+    is the identity."""
+    ids, mask, pos = make_batch(2, 3, 7, 4, 50, 21, resp_len_range=(1, 4))
+    groups, uniq = oracle.find_prompt_groups(ids, 4, mask)
+    x = np.random.default_rng(9).standard_normal(ids.shape + (2,))
+    for unpad in (False, True):
+        _, _, info = oracle.create_deduplicated_batch(ids, pos, 4, groups, uniq, attention_mask=mask,
+                                                      use_unpad=unpad)
+        back = oracle.pack_rows_backward(pack_rows(x, info), info)
+        for g in groups:
+            rep, others = g[0], g[1:]
+            keep = np.ones(ids.shape[1], bool) if not unpad else mask[rep] != 0
+            assert np.array_equal(back[rep][keep], x[rep][keep])
+            assert not back[rep][~keep].any()
+            for b in others:
+                assert not back[b, :7].any()
+                keep_r = np.ones(4, bool) if not unpad else mask[b, 7:] != 0
+                assert np.array_equal(back[b, 7:][keep_r], x[b, 7:][keep_r])
+                assert not back[b, 7:][~keep_r].any()
+    ids, mask, pos = make_batch(5, 1, 8, 4, 1000, 3)
+    groups, uniq = oracle.find_prompt_groups(ids, 4, mask)
+    _, _, info = oracle.create_deduplicated_batch(ids, pos, 4, groups, uniq)
+    x = np.random.default_rng(10).standard_normal(ids.shape + (2,))
+    assert np.array_equal(oracle.pack_rows_backward(pack_rows(x, info), info), x)
+
+
 def test_batch_stats_closed_form():
     """A batch built with known lengths: 3 rows, L = 10, response_length 4.
     Prompts hold 6, 4 and 6 valid tokens (left padded); responses 4, 0 and 2
