@@ -68,8 +68,15 @@ int64_t zr_kernel_launches(void);
 /* Test and tuning knobs (process-wide, not thread-safe; set before use):
  *  "weak_hash"   1 = every prompt hashes to the same value (forces the exact
  *                row comparison to resolve all groups; results are unchanged)
- *  "wait_limit"  bounded-wait limit of the tensor-core kernels in polls
- *                (0 = default, about a second)
+ *  "wait_limit"  bounded-wait limit of the tensor-core kernels in SM clock
+ *                cycles (0 = default, 4e9 cycles: about two seconds)
+ *  "test_withhold_arrival"  test option: bit 0 makes the forward skip the
+ *                Q load of its first work unit, bit 1 makes the backward skip
+ *                the K/V load of its first work unit (in whichever CTA takes
+ *                that unit).  The wait on that load runs out
+ *                after "wait_limit" cycles, the CTA leaves cleanly and
+ *                zr_check_status reports ZR_ERR_TIMEOUT; the outputs of that
+ *                call are incomplete.  0 = off (the only production value)
  *  "kernel_timing" 1 = record a CUDA event pair on the launch stream around
  *                every launch of the kernels named under zr_kernel_time
  *                (a few microseconds of host work per launch; 0 = off)
@@ -81,8 +88,10 @@ zr_status zr_set_option(const char* name, int64_t value);
  * events recorded on the stream it is launched on.  zr_kernel_time waits for
  * the recorded pairs filed under `name` and returns their summed elapsed time
  * in milliseconds and their count.  Names: "attn_fwd", "attn_bwd_prep",
- * "attn_dkdv", "attn_dq" (tensor-core attention), "pack_gather",
- * "reconstruct" (row copies).  An unknown name yields 0 launches.
+ * "attn_bwd", "attn_dq_convert" (tensor-core attention), "pack_gather",
+ * "reconstruct", "reconstruct_backward", "pack_backward",
+ * "reconstruct_pack_backward" (row copies).  An unknown name yields 0
+ * launches.
  * At most 16384 pairs are kept; pairs past that are dropped and the call
  * returns ZR_ERR_CAPACITY (with the sums of the kept pairs written).
  * zr_kernel_time_reset waits for and forgets every recorded pair.  Both are
@@ -272,6 +281,35 @@ zr_status zr_reconstruct(const zr_recon_info* info, const void* packed, int64_t 
 zr_status zr_reconstruct_backward(const zr_recon_info* info, const void* grad_out, int64_t W, int dtype,
                                   void* grad_packed, void* stream);
 
+/* The adjoint of zr_pack_rows / the pack of zr_pack_dedup ("Correctness &
+ * Gradients": gradients flow back through the deduplication step as well as
+ * the reconstruction).  Source position (b, p) receives the gradient of the
+ * packed row that was read from it; each position is read at most once, so
+ * this is a copy (any element type, rows of row_bytes bytes).  Positions the
+ * pack never read -- the prompt rows of every group member other than its
+ * representative (the first member), and the pads that use_unpad dropped --
+ * are zero-filled.
+ *  grad_packed  [T_cap, row_bytes] device; rows [0, T) read
+ *  grad_src     [B, L, row_bytes] device; every position written
+ * Async on `stream`. */
+zr_status zr_pack_rows_backward(const zr_recon_info* info, const void* grad_packed, int64_t row_bytes,
+                                void* grad_src, void* stream);
+
+/* The gradient of zr_reconstruct(zr_pack_rows(x)) with respect to x, in one
+ * pass without the packed intermediate: the composition of
+ * zr_reconstruct_backward and zr_pack_rows_backward, for a tensor that enters
+ * the deduplicated section packed and leaves it reconstructed unchanged (a
+ * skip connection around it).  The representative's prompt positions that
+ * the pack read receive the fp32 sum, over the group's members in group
+ * order, of grad_out there, rounded once to the element type; every row's
+ * packed response positions pass their own gradient through; all other
+ * positions are zero.  Bitwise equal to the two calls in sequence.
+ *  grad_out  [B, L, W] elements of `dtype` (ZR_BF16 or ZR_F32), device
+ *  grad_in   [B, L, W] of the same type, device; must not alias grad_out
+ * Async on `stream`. */
+zr_status zr_reconstruct_pack_backward(const zr_recon_info* info, const void* grad_out, int64_t W,
+                                       int dtype, void* grad_in, void* stream);
+
 /* -------------------------------------------------------------------------
  * Batch statistics of a normal (not deduplicated) batch ("Debugging &
  * Analysis", "Batch Statistics"): prompt length, response count with
@@ -313,9 +351,13 @@ zr_status zr_batch_stats_compute(const uint8_t* attention_mask, int B, int L, in
  *  D             head dimension: 64 or 128 for ZR_BF16; 32, 64, 96 or 128
  *                for ZR_F32 (other values: ZR_ERR_UNSUPPORTED)
  *  softmax_scale <= 0 selects 1/sqrt(D)
- *  workspace     zr_split_attn_workspace(info, Hq, Hkv, D) bytes, 256-aligned
+ *  workspace     zr_split_attn_workspace(info, Hq, Hkv, D) bytes, 256-aligned;
+ *                it includes the backward's fp32 dQ accumulator
+ *                (T_cap * Hq * D * 4 bytes)
  * The backward takes o and lse from the forward and recomputes the attention
- * probabilities from lse.
+ * probabilities from lse.  Its dQ sums fp32 partials from different key
+ * tiles in arrival order, so the last bits of dq can differ between runs;
+ * o, lse, dk and dv are bitwise reproducible.
  */
 size_t zr_split_attn_workspace(const zr_recon_info* info, int Hq, int Hkv, int D);
 

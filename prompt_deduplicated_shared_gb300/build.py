@@ -68,7 +68,7 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(run, jobs))
     if jobs or not os.path.exists(LIB):
-        link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", LIB + ".tmp", *objs]
+        link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", LIB + ".tmp", *objs, "-ldl"]
         run(link)
         os.replace(LIB + ".tmp", LIB)
     return LIB

@@ -137,6 +137,9 @@ zr_status zr_set_option(const char* name, int64_t value) {
         options().wait_limit = value;
     } else if (!strcmp(name, "kernel_timing")) {
         options().kernel_timing = value != 0;
+    } else if (!strcmp(name, "test_withhold_arrival")) {
+        if (value < 0 || value > 3) return set_error(ZR_ERR_INVALID_ARG, "test_withhold_arrival must be 0..3");
+        options().test_withhold = (int)value;
     } else {
         return set_error(ZR_ERR_INVALID_ARG, "unknown option '%s'", name);
     }
@@ -186,6 +189,7 @@ zr_status zr_find_prompt_groups(const int64_t* input_ids, const uint8_t* attenti
                                 int L, int response_length, const zr_groups* out,
                                 int64_t* unique_prompts, int32_t* num_groups_host, void* workspace,
                                 size_t workspace_bytes, void* stream) {
+    ZR_NVTX("zr_find_prompt_groups");
     if (!input_ids || !out || !out->group_ptr || !out->members || !out->group_of || !out->num_groups)
         return set_error(ZR_ERR_INVALID_ARG, "NULL input_ids or group output");
     if (B <= 0 || L <= 0) return set_error(ZR_ERR_INVALID_ARG, "B and L must be positive (B=%d L=%d)", B, L);
@@ -261,6 +265,7 @@ zr_status zr_pack_dedup(const int64_t* input_ids, const int64_t* position_ids,
                         const uint8_t* attention_mask, const zr_groups* groups,
                         int64_t* dedup_input_ids, int64_t* dedup_position_ids, uint8_t* dedup_mask,
                         zr_recon_info* info, int64_t* T_host, void* stream) {
+    ZR_NVTX("zr_pack_dedup");
     zr_status st = check_info(info);
     if (st != ZR_OK) return st;
     if (!input_ids || !groups || !groups->group_ptr || !groups->members || !groups->group_of ||
@@ -306,6 +311,7 @@ zr_status zr_pack_dedup(const int64_t* input_ids, const int64_t* position_ids,
 
 zr_status zr_pack_rows(const zr_recon_info* info, const void* src, int64_t row_bytes, void* dst,
                        void* stream) {
+    ZR_NVTX("zr_pack_rows");
     zr_status st = check_info(info);
     if (st != ZR_OK) return st;
     if (!src || !dst || row_bytes <= 0) return set_error(ZR_ERR_INVALID_ARG, "NULL src/dst or row_bytes <= 0");
@@ -314,6 +320,7 @@ zr_status zr_pack_rows(const zr_recon_info* info, const void* src, int64_t row_b
 
 zr_status zr_reconstruct(const zr_recon_info* info, const void* packed, int64_t row_bytes, void* out,
                          void* stream) {
+    ZR_NVTX("zr_reconstruct");
     zr_status st = check_info(info);
     if (st != ZR_OK) return st;
     if (!packed || !out || row_bytes <= 0)
@@ -323,6 +330,7 @@ zr_status zr_reconstruct(const zr_recon_info* info, const void* packed, int64_t 
 
 zr_status zr_reconstruct_backward(const zr_recon_info* info, const void* grad_out, int64_t W, int dtype,
                                   void* grad_packed, void* stream) {
+    ZR_NVTX("zr_reconstruct_backward");
     zr_status st = check_info(info);
     if (st != ZR_OK) return st;
     if (!grad_out || !grad_packed || W <= 0)
@@ -333,6 +341,29 @@ zr_status zr_reconstruct_backward(const zr_recon_info* info, const void* grad_ou
                                        static_cast<cudaStream_t>(stream));
 }
 
+zr_status zr_pack_rows_backward(const zr_recon_info* info, const void* grad_packed, int64_t row_bytes,
+                                void* grad_src, void* stream) {
+    ZR_NVTX("zr_pack_rows_backward");
+    zr_status st = check_info(info);
+    if (st != ZR_OK) return st;
+    if (!grad_packed || !grad_src || row_bytes <= 0)
+        return set_error(ZR_ERR_INVALID_ARG, "NULL grad_packed/grad_src or row_bytes <= 0");
+    return launch_pack_backward(*info, grad_packed, row_bytes, grad_src, static_cast<cudaStream_t>(stream));
+}
+
+zr_status zr_reconstruct_pack_backward(const zr_recon_info* info, const void* grad_out, int64_t W, int dtype,
+                                       void* grad_in, void* stream) {
+    ZR_NVTX("zr_reconstruct_pack_backward");
+    zr_status st = check_info(info);
+    if (st != ZR_OK) return st;
+    if (!grad_out || !grad_in || W <= 0) return set_error(ZR_ERR_INVALID_ARG, "NULL grad_out/grad_in or W <= 0");
+    if (grad_out == grad_in) return set_error(ZR_ERR_INVALID_ARG, "grad_in must not alias grad_out");
+    if (dtype != ZR_BF16 && dtype != ZR_F32)
+        return set_error(ZR_ERR_UNSUPPORTED, "reconstruct_pack_backward supports ZR_BF16 and ZR_F32 elements");
+    return launch_reconstruct_pack_backward(*info, grad_out, W, static_cast<zr_dtype>(dtype), grad_in,
+                                            static_cast<cudaStream_t>(stream));
+}
+
 size_t zr_batch_stats_workspace(int B) {
     if (B <= 0) return 0;
     return 2 * align256((size_t)B * 4) + align256(16) + align256(sizeof(zr_batch_stats));
@@ -340,6 +371,7 @@ size_t zr_batch_stats_workspace(int B) {
 
 zr_status zr_batch_stats_compute(const uint8_t* attention_mask, int B, int L, int response_length,
                                  zr_batch_stats* out, void* workspace, size_t workspace_bytes, void* stream) {
+    ZR_NVTX("zr_batch_stats_compute");
     if (!out) return set_error(ZR_ERR_INVALID_ARG, "NULL output");
     if (B <= 0 || L <= 0 || response_length < 0 || response_length > L)
         return set_error(ZR_ERR_INVALID_ARG, "bad sizes B=%d L=%d response_length=%d", B, L, response_length);
@@ -386,6 +418,7 @@ zr_status zr_split_attn_fwd(const zr_recon_info* info, const void* q, const void
                             void* o, float* lse, int Hq, int Hkv, int D, zr_dtype dtype,
                             float softmax_scale, void* workspace, size_t workspace_bytes,
                             void* stream) {
+    ZR_NVTX("zr_split_attn_fwd");
     AttnWorkspace ws;
     zr_status st = attn_common(info, Hq, Hkv, D, dtype, workspace, workspace_bytes, &ws);
     if (st != ZR_OK) return st;
@@ -416,6 +449,7 @@ zr_status zr_split_attn_bwd(const zr_recon_info* info, const void* q, const void
                             const void* o, const float* lse, const void* dout, void* dq, void* dk,
                             void* dv, int Hq, int Hkv, int D, zr_dtype dtype, float softmax_scale,
                             void* workspace, size_t workspace_bytes, void* stream) {
+    ZR_NVTX("zr_split_attn_bwd");
     AttnWorkspace ws;
     zr_status st = attn_common(info, Hq, Hkv, D, dtype, workspace, workspace_bytes, &ws);
     if (st != ZR_OK) return st;
@@ -450,6 +484,7 @@ zr_status zr_split_attn_bwd(const zr_recon_info* info, const void* q, const void
 }
 
 zr_status zr_check_status(const zr_recon_info* info, void* attn_workspace, void* stream) {
+    ZR_NVTX("zr_check_status");
     zr_status st = check_info(info);
     if (st != ZR_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

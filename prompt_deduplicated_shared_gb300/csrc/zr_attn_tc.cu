@@ -92,6 +92,7 @@ struct FwdParams {
     int* status;
     int* sched;       // global unit counter (zeroed by the plan kernel)
     long long limit;
+    int withhold;     // test option: the Q load of unit 0 is skipped
 };
 
 // Query heads of pair hp (slot 1 repeats the last head when Hq is odd) and
@@ -186,7 +187,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            int kstage = 0, k = 0;
+            int kstage = 0, k = 0, last_q = -1;
             bool ok = true;
             for (; ok; ++k) {
                 const int u = ring_publish(ring, k, p.sched, n_units, ab);
@@ -197,11 +198,16 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const PairHeads ph = pair_heads(hp, p.Hq, p.ratio);
                 const int W = ph.split ? 2 : 1;
                 if (k > 0 && !mbar_wait(b_qempty, (k - 1) & 1, ab, 1)) { ok = false; break; }
-                mbar_expect_tx(b_qfull, 2 * C::kQBytes);
+                // test option: the CTA that takes unit 0 withholds its Q load, so
+                // that a bounded wait runs out and the abort path runs
+                if (!(p.withhold && u == 0)) {
+                    mbar_expect_tx(b_qfull, 2 * C::kQBytes);
 #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_2d(sQ0 + c * kChunkBytes, &tm_q, ph.h[0] * D + 64 * c, t.q0, b_qfull);
-                    tma_load_2d(sQ1 + c * kChunkBytes, &tm_q, ph.h[1] * D + 64 * c, t.q0, b_qfull);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_2d(sQ0 + c * kChunkBytes, &tm_q, ph.h[0] * D + 64 * c, t.q0, b_qfull);
+                        tma_load_2d(sQ1 + c * kChunkBytes, &tm_q, ph.h[1] * D + 64 * c, t.q0, b_qfull);
+                    }
+                    last_q = k;
                 }
                 const int npb = cdiv128(t.pk1 - t.pk0);
                 const int n = t.nblk;
@@ -226,11 +232,18 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 for (int w = 0; w < W && ok; ++w) ok = load(&tm_v, ph.hk[w], key_block_row(t, npb, n - 1));
                 if (!ok) break;
             }
-            // drain: every load consumed and every commit landed before exit
             const long long lim = p.limit;
-            for (int s = kstage - C::kStages; s < kstage; ++s)
-                if (s >= 0) mbar_wait_drain(b_kvempty(s % C::kStages), (s / C::kStages) & 1, lim);
-            if (k > 0) mbar_wait_drain(b_qempty, (k - 1) & 1, lim);
+            if (ok) {
+                // every load consumed and every release committed before exit
+                for (int s = kstage - C::kStages; s < kstage; ++s)
+                    if (s >= 0) mbar_wait_drain(b_kvempty(s % C::kStages), (s / C::kStages) & 1, lim);
+                if (k > 0) mbar_wait_drain(b_qempty, (k - 1) & 1, lim);
+            } else {
+                // abort: the consumers have left; wait until the copies in flight landed
+                for (int s = kstage - C::kStages; s < kstage; ++s)
+                    if (s >= 0) mbar_wait_drain(b_kvfull(s % C::kStages), (s / C::kStages) & 1, lim);
+                if (last_q >= 0) mbar_wait_drain(b_qfull, last_q & 1, lim);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -503,6 +516,7 @@ zr_status launch_fwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     p.status = info.status + kStatusTimeout;  // read by zr_check_status(info)
     p.sched = ws.plan.counts + 2;
     p.limit = wait_limit_cycles();
+    p.withhold = (options().test_withhold & 1) != 0;
     ZR_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::kSmemBytes));
     {

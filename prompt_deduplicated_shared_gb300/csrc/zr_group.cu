@@ -301,6 +301,7 @@ extern "C" zr_status zr_find_prompt_groups_noalloc(const int64_t* input_ids, con
                                                    int64_t* unique_prompts, int32_t* num_groups_host,
                                                    void* stream) {
     using namespace zr;
+    ZR_NVTX("zr_find_prompt_groups_noalloc");
     if (!input_ids || !out || !out->group_ptr || !out->members || !out->group_of || !out->num_groups)
         return set_error(ZR_ERR_INVALID_ARG, "NULL input_ids or group output");
     if (B <= 0 || L <= 0) return set_error(ZR_ERR_INVALID_ARG, "B and L must be positive (B=%d L=%d)", B, L);
@@ -344,6 +345,7 @@ __global__ void identity_groups_kernel(int B, int32_t* __restrict__ group_ptr, i
 
 extern "C" zr_status zr_identity_groups(int B, const zr_groups* out, void* stream) {
     using namespace zr;
+    ZR_NVTX("zr_identity_groups");
     if (!out || !out->group_ptr || !out->members || !out->group_of || !out->num_groups)
         return set_error(ZR_ERR_INVALID_ARG, "NULL group output");
     if (B <= 0) return set_error(ZR_ERR_INVALID_ARG, "B must be positive (B=%d)", B);

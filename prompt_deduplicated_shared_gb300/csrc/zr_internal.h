@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "zr.h"
@@ -19,6 +20,18 @@ zr_status cuda_error(cudaError_t e, const char* what);
     } while (0)
 
 void count_launch();
+
+// An NVTX range named after the entry point, open for the duration of the
+// call (profilers show each zr_* call on the host timeline; without a tool
+// attached the push and pop cost a few nanoseconds).
+class NvtxRange {
+public:
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define ZR_NVTX(name) ::zr::NvtxRange zr_nvtx_range_(name)
 
 #define ZR_LAUNCH_CHECK(what)                               \
     do {                                                    \
@@ -46,6 +59,7 @@ struct Options {
     int weak_hash = 0;
     int64_t wait_limit = 0;
     int kernel_timing = 0;
+    int test_withhold = 0;   // bit 0: forward, bit 1: backward (test option)
 };
 Options& options();
 
@@ -67,6 +81,10 @@ zr_status launch_reconstruct(const zr_recon_info& info, const void* packed, int6
                              void* out, cudaStream_t s);
 zr_status launch_reconstruct_backward(const zr_recon_info& info, const void* grad_out, int64_t W,
                                       zr_dtype dtype, void* grad_packed, cudaStream_t s);
+zr_status launch_pack_backward(const zr_recon_info& info, const void* grad_packed, int64_t row_bytes,
+                               void* grad_src, cudaStream_t s);
+zr_status launch_reconstruct_pack_backward(const zr_recon_info& info, const void* grad_out, int64_t W,
+                                           zr_dtype dtype, void* grad_in, cudaStream_t s);
 zr_status launch_batch_stats(const uint8_t* mask, int B, int L, int P, int32_t* plen, int32_t* rlen,
                              int32_t* status, zr_batch_stats* dev_out, cudaStream_t s);
 // zero the pad rows (padded mode) of a [T_cap, row_bytes] packed tensor
@@ -117,7 +135,7 @@ struct AttnWorkspace {
     float* delta;        // [T_cap, Hq] rowsum(dO * O), backward only (SIMT)
     float* delta_t;      // [Hq, T_cap] rowsum(dO * O), backward only (tensor cores)
     float* lse2_t;       // [Hq, T_cap] log-sum-exp in base 2, backward only (tensor cores)
-    float* dq_accum;     // [T_cap, Hq, D] fp32, backward only (optional)
+    float* dq_accum;     // [T_cap, Hq, D] fp32, tensor-core backward only
     size_t bytes;
 };
 

@@ -500,6 +500,13 @@ __global__ void __launch_bounds__(256) reconstruct_backward_kernel(const ElemT* 
 // Each item intersects its row range with the four reconstruction segments of
 // row b (prompt pad, prompt, response, response pad) and copies or zero-fills
 // the overlaps.  Persistent blocks stride over the items.
+//
+// With kPackAdjoint the same walk computes the adjoint of the pack: source
+// position (b, p) receives the gradient of the packed row that was read from
+// it.  The pack reads a group's prompt from its representative (the first
+// member) only, so the prompt segment of every other member is zero-filled;
+// everything else is the reconstruction's copy.
+template <bool kPackAdjoint>
 __global__ void __launch_bounds__(256) reconstruct_rows_kernel(const char* __restrict__ packed,
                                                                char* __restrict__ out,
                                                                zr_recon_info info, int chunk_rows,
@@ -515,16 +522,97 @@ __global__ void __launch_bounds__(256) reconstruct_rows_kernel(const char* __res
         const int64_t local = k - (int64_t)base * nchunks;
         const int64_t c = local / n;
         const int b = info.members[base + (int)(local % n)];
+        const bool rep = b == info.members[base];
         const int64_t r0 = c * chunk_rows;
         const int64_t r1 = min((int64_t)L, r0 + chunk_rows);
         const int64_t row0 = (int64_t)b * L;
         for (int sgi = 0; sgi < 4; ++sgi) {
             const int64_t* seg = info.recon_segs + 3 * (4 * (int64_t)b + sgi);
-            const int64_t src = seg[0], lo = seg[1] - row0, nrows = seg[2];
+            const int64_t src = (kPackAdjoint && sgi == 0 && !rep) ? -1 : seg[0];
+            const int64_t lo = seg[1] - row0, nrows = seg[2];
             const int64_t a = max(lo, r0), e = min(lo + nrows, r1);
             if (a >= e) continue;
             block_copy<true>(src >= 0 ? packed + (src + (a - lo)) * row_bytes : nullptr,
                              out + (row0 + a) * row_bytes, (e - a) * row_bytes);
+        }
+    }
+}
+
+// The gradient of reconstruct(pack(x)) with respect to x in one pass, for a
+// tensor that is packed, carried unchanged and reconstructed (the adjoint of
+// the reconstruction followed by the adjoint of the pack, without the packed
+// intermediate).  Output-stationary over [B, L] like the reconstruction: the
+// representative of a group receives, at each prompt position the pack read,
+// the fp32 sum over the group's members (in group order, rounded once) of
+// grad_out there; the prompt rows of the other members are zero; every row's
+// packed response positions pass their own gradient through; positions the
+// pack dropped or never read are zero.
+template <typename ElemT>
+__global__ void __launch_bounds__(256) reconstruct_pack_backward_kernel(const ElemT* __restrict__ gout,
+                                                                        ElemT* __restrict__ gin,
+                                                                        zr_recon_info info, int chunk_rows,
+                                                                        int64_t nchunks, int64_t W) {
+    const int L = info.L;
+    const int64_t row_bytes = W * (int64_t)sizeof(ElemT);
+    constexpr int kPerVec = 16 / sizeof(ElemT);
+    const bool vec = (row_bytes & 15) == 0 && (((uintptr_t)gout | (uintptr_t)gin) & 15) == 0;
+    const int64_t items = (int64_t)info.B * nchunks;
+    for (int64_t k = blockIdx.x; k < items; k += gridDim.x) {
+        const int q = (int)(k / nchunks);
+        const int g = info.group_of[info.members[q]];
+        const int base = info.group_ptr[g];
+        const int n = info.group_ptr[g + 1] - base;
+        if (n <= 0) continue;
+        const int64_t local = k - (int64_t)base * nchunks;
+        const int64_t c = local / n;
+        const int b = info.members[base + (int)(local % n)];
+        const bool rep = b == info.members[base];
+        const int64_t r0 = c * chunk_rows;
+        const int64_t r1 = min((int64_t)L, r0 + chunk_rows);
+        const int64_t row0 = (int64_t)b * L;
+        for (int sgi = 0; sgi < 4; ++sgi) {
+            const int64_t* seg = info.recon_segs + 3 * (4 * (int64_t)b + sgi);
+            const int64_t lo = seg[1] - row0, nrows = seg[2];
+            const int64_t a = max(lo, r0), e = min(lo + nrows, r1);
+            if (a >= e) continue;
+            char* dst = reinterpret_cast<char*>(gin + (row0 + a) * W);
+            if (seg[0] < 0 || (sgi == 0 && !rep)) {  // pads, other members' prompts
+                block_copy<false>(nullptr, dst, (e - a) * row_bytes);
+                continue;
+            }
+            if (sgi == 2) {  // the row's own response rows
+                block_copy<false>(reinterpret_cast<const char*>(gout + (row0 + a) * W), dst, (e - a) * row_bytes);
+                continue;
+            }
+            // the representative's prompt rows: sum over the group's members
+            const int64_t nel = (e - a) * W;
+            ElemT* d = gin + (row0 + a) * W;
+            if (vec) {
+                const int64_t nv = nel / kPerVec;
+                for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
+                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    int m = base;
+                    for (; m + 4 <= base + n; m += 4) {
+                        uint4 x[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            x[u] = __ldg(reinterpret_cast<const uint4*>(gout + ((int64_t)info.members[m + u] * L + a) * W) + v);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) acc16(acc, x[u], ElemT());
+                    }
+                    for (; m < base + n; ++m)
+                        acc16(acc, __ldg(reinterpret_cast<const uint4*>(gout + ((int64_t)info.members[m] * L + a) * W) + v),
+                              ElemT());
+                    reinterpret_cast<uint4*>(d)[v] = out16(acc, ElemT());
+                }
+            } else {
+                for (int64_t v = threadIdx.x; v < nel; v += blockDim.x) {
+                    float acc = 0.f;
+                    for (int m = base; m < base + n; ++m)
+                        acc += elem_to_f(gout[((int64_t)info.members[m] * L + a) * W + v]);
+                    f_to_elem(acc, d + v);
+                }
+            }
         }
     }
 }
@@ -650,10 +738,43 @@ zr_status launch_reconstruct(const zr_recon_info& info, const void* packed, int6
     const int64_t items = (int64_t)info.B * nchunks;
     const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * 8);
     KernelTimer timer("reconstruct", s);
-    reconstruct_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const char*>(packed),
-                                                 static_cast<char*>(out), info, chunk_rows, nchunks,
-                                                 row_bytes);
+    reconstruct_rows_kernel<false><<<grid, 256, 0, s>>>(static_cast<const char*>(packed),
+                                                        static_cast<char*>(out), info, chunk_rows, nchunks,
+                                                        row_bytes);
     ZR_LAUNCH_CHECK("reconstruct_rows_kernel");
+    return ZR_OK;
+}
+
+zr_status launch_pack_backward(const zr_recon_info& info, const void* grad_packed, int64_t row_bytes,
+                               void* grad_src, cudaStream_t s) {
+    const int chunk_rows = (int)std::max<int64_t>(1, std::min<int64_t>(info.L, 32768 / row_bytes));
+    const int64_t nchunks = (info.L + chunk_rows - 1) / chunk_rows;
+    const int64_t items = (int64_t)info.B * nchunks;
+    const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * 8);
+    KernelTimer timer("pack_backward", s);
+    reconstruct_rows_kernel<true><<<grid, 256, 0, s>>>(static_cast<const char*>(grad_packed),
+                                                       static_cast<char*>(grad_src), info, chunk_rows, nchunks,
+                                                       row_bytes);
+    ZR_LAUNCH_CHECK("reconstruct_rows_kernel(pack adjoint)");
+    return ZR_OK;
+}
+
+zr_status launch_reconstruct_pack_backward(const zr_recon_info& info, const void* grad_out, int64_t W,
+                                           zr_dtype dtype, void* grad_in, cudaStream_t s) {
+    const int64_t row_bytes = W * (dtype == ZR_F32 ? 4 : 2);
+    const int chunk_rows = (int)std::max<int64_t>(1, std::min<int64_t>(info.L, 32768 / row_bytes));
+    const int64_t nchunks = (info.L + chunk_rows - 1) / chunk_rows;
+    const int64_t items = (int64_t)info.B * nchunks;
+    const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * 8);
+    KernelTimer timer("reconstruct_pack_backward", s);
+    if (dtype == ZR_F32)
+        reconstruct_pack_backward_kernel<float><<<grid, 256, 0, s>>>(
+            static_cast<const float*>(grad_out), static_cast<float*>(grad_in), info, chunk_rows, nchunks, W);
+    else
+        reconstruct_pack_backward_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(grad_out), static_cast<__nv_bfloat16*>(grad_in), info, chunk_rows,
+            nchunks, W);
+    ZR_LAUNCH_CHECK("reconstruct_pack_backward_kernel");
     return ZR_OK;
 }
 

@@ -95,6 +95,9 @@ def lib():
         "zr_reconstruct": (ctypes.c_int, [ctypes.POINTER(ZrReconInfoC), _vp, _i64, _vp, _vp]),
         "zr_reconstruct_backward": (ctypes.c_int, [ctypes.POINTER(ZrReconInfoC), _vp, _i64, ctypes.c_int, _vp,
                                                    _vp]),
+        "zr_pack_rows_backward": (ctypes.c_int, [ctypes.POINTER(ZrReconInfoC), _vp, _i64, _vp, _vp]),
+        "zr_reconstruct_pack_backward": (ctypes.c_int, [ctypes.POINTER(ZrReconInfoC), _vp, _i64, ctypes.c_int,
+                                                        _vp, _vp]),
         "zr_batch_stats_workspace": (ctypes.c_size_t, [ctypes.c_int]),
         "zr_batch_stats_compute": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                   ctypes.POINTER(ZrBatchStatsC), _vp, ctypes.c_size_t, _vp]),
@@ -367,6 +370,30 @@ def reconstruct_backward(info: ReconInfo, grad_out, out=None):
                                                   dtype=grad_out.dtype, device=grad_out.device)
     _check(lib().zr_reconstruct_backward(ctypes.byref(info.c), _p(grad_out), W, dt, _p(dst),
                                          _stream(grad_out.device)))
+    return dst
+
+
+def pack_rows_backward(info: ReconInfo, grad_packed, out=None):
+    """zr_pack_rows_backward: the adjoint of pack_rows, ``[T_cap, ...]`` ->
+    ``[B, L, ...]`` (any dtype); positions the pack never read are zero."""
+    _dev(grad_packed, out)
+    row_bytes = grad_packed[0].numel() * grad_packed.element_size()
+    dst = out if out is not None else torch.empty((info.B, info.L) + tuple(grad_packed.shape[1:]),
+                                                  dtype=grad_packed.dtype, device=grad_packed.device)
+    _check(lib().zr_pack_rows_backward(ctypes.byref(info.c), _p(grad_packed), row_bytes, _p(dst),
+                                       _stream(grad_packed.device)))
+    return dst
+
+
+def reconstruct_pack_backward(info: ReconInfo, grad_out, out=None):
+    """zr_reconstruct_pack_backward: the gradient of reconstruct(pack_rows(x))
+    with respect to x in one pass, ``[B, L, ...]`` -> ``[B, L, ...]`` (bf16 or
+    fp32)."""
+    _dev(grad_out, out)
+    W = grad_out[0, 0].numel()
+    dst = out if out is not None else torch.empty_like(grad_out)
+    _check(lib().zr_reconstruct_pack_backward(ctypes.byref(info.c), _p(grad_out), W, _dtype_code(grad_out),
+                                              _p(dst), _stream(grad_out.device)))
     return dst
 
 

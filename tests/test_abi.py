@@ -42,6 +42,8 @@ def test_version_and_options(zr):
     assert lib.zr_set_option(b"attn_impl", 0) == zr.ZR_ERR_INVALID_ARG
     assert lib.zr_set_option(b"wait_limit", -1) == zr.ZR_ERR_INVALID_ARG
     assert lib.zr_set_option(b"wait_limit", 0) == zr.ZR_OK
+    assert lib.zr_set_option(b"test_withhold_arrival", 4) == zr.ZR_ERR_INVALID_ARG
+    assert lib.zr_set_option(b"test_withhold_arrival", 0) == zr.ZR_OK
 
 
 def test_kernel_time_without_records(zr):

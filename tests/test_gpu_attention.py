@@ -42,13 +42,13 @@ def _run(zr, info, tq, tk, tv, tdo, backward=True):
         grads = zr.split_attn_bwd(info, tq, tk, tv, o, lse, tdo) if backward else None
         torch.cuda.synchronize()
         zr.check_status(info)
-        launched = {n: zr.kernel_time(n)[1] for n in ("attn_fwd", "attn_dkdv")}
+        launched = {n: zr.kernel_time(n)[1] for n in ("attn_fwd", "attn_bwd")}
     finally:
         zr.set_option("kernel_timing", 0)
         zr.kernel_time_reset()
     tc = _tc_expected(tq.dtype, tq.shape[2])
     assert launched["attn_fwd"] == (1 if tc else 0), launched
-    assert launched["attn_dkdv"] == (1 if tc and backward else 0), launched
+    assert launched["attn_bwd"] == (1 if tc and backward else 0), launched
     return o, lse, grads
 
 
@@ -180,15 +180,19 @@ def test_kernel_timing_counts_launches_and_changes_nothing(zr):
     zr.set_option("kernel_timing", 1)
     try:
         timed = plain_run()
-        times = {n: zr.kernel_time(n) for n in ("attn_fwd", "attn_bwd_prep", "attn_dkdv", "attn_dq")}
+        times = {n: zr.kernel_time(n) for n in ("attn_fwd", "attn_bwd_prep", "attn_bwd", "attn_dq_convert")}
     finally:
         zr.set_option("kernel_timing", 0)
         zr.kernel_time_reset()
     for n, (ms, count) in times.items():
         assert count == 1 and ms > 0.0, (n, ms, count)
     assert torch.equal(plain[0], timed[0]) and torch.equal(plain[1], timed[1])
-    for a, b in zip(plain[2], timed[2]):
-        assert torch.equal(a, b)
+    # dK and dV accumulate in a fixed order; dQ sums partials from different
+    # CTAs in fp32 in arrival order, so two runs may differ in the last bits
+    dq0, dk0, dv0 = plain[2]
+    dq1, dk1, dv1 = timed[2]
+    assert torch.equal(dk0, dk1) and torch.equal(dv0, dv1)
+    assert float((dq0.float() - dq1.float()).abs().max()) <= 2.0 ** -7 * float(dq0.float().abs().max())
     assert zr.kernel_time("attn_fwd") == (0.0, 0)
 
 

@@ -232,3 +232,79 @@ def test_batch_stats_full_size(zr):
     got = zr.batch_stats(torch.from_numpy(ids).to(DEV), torch.from_numpy(mask).to(DEV), wl.R)
     assert got == oracle.batch_stats(mask, wl.R)
     assert got["responses"] == wl.B and 256 <= got["resp_len_min"] <= got["resp_len_max"] <= 1024
+
+
+def _check_pack_backward(zr, ginfo, info, ids_shape, width, dtype, seed):
+    """The pack adjoint is a copy: bit-exact against the oracle, every
+    position written (unread ones zero)."""
+    T = info.T
+    gp = torch.from_numpy(np.random.default_rng(seed).standard_normal((ginfo.T_cap, width)).astype(np.float32))
+    gp = gp.to(DEV, dtype)
+    got = zr.pack_rows_backward(ginfo, gp)
+    torch.cuda.synchronize()
+    zr.check_status(ginfo)
+    ref = oracle.pack_rows_backward(gp[:T].float().cpu().numpy(), info)
+    assert tuple(got.shape) == tuple(ids_shape) + (width,)
+    assert np.array_equal(got.float().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("use_unpad", [False, True])
+@pytest.mark.parametrize("width,dtype", [(3, torch.float32), (40, torch.bfloat16), (1, torch.bfloat16)],
+                         ids=["f32-3", "bf16-40", "bf16-1"])
+@pytest.mark.parametrize("name,kw", [CASES[1], CASES[2], CASES[3], CASES[5], CASES[6], CASES[8]],
+                         ids=[CASES[i][0] for i in (1, 2, 3, 5, 6, 8)])
+def test_pack_rows_backward_small(zr, name, kw, use_unpad, width, dtype):
+    ids, mask, pos = make_batch(**kw)
+    R = kw["R"]
+    if use_unpad and mask is None:
+        mask = np.ones_like(ids, dtype=np.uint8)
+    ginfo, info, T = _check_pack(zr, ids, mask, pos, R, use_unpad)
+    _check_pack_backward(zr, ginfo, info, ids.shape, width, dtype, 12)
+
+
+@pytest.mark.parametrize("use_unpad", [False, True])
+@pytest.mark.parametrize("width,dtype", [(24, torch.float32), (3, torch.float32), (40, torch.bfloat16),
+                                         (5, torch.bfloat16)], ids=["f32-24", "f32-3", "bf16-40", "bf16-5"])
+@pytest.mark.parametrize("name,kw", [CASES[2], CASES[3], CASES[5], CASES[6], CASES[8]],
+                         ids=[CASES[i][0] for i in (2, 3, 5, 6, 8)])
+def test_reconstruct_pack_backward_small(zr, name, kw, use_unpad, width, dtype):
+    """The fused round-trip gradient: bitwise equal to the reconstruction
+    adjoint followed by the pack adjoint on the GPU, and within the fp32
+    summation bound of the oracle's composition of the two."""
+    ids, mask, pos = make_batch(**kw)
+    R = kw["R"]
+    if use_unpad and mask is None:
+        mask = np.ones_like(ids, dtype=np.uint8)
+    ginfo, info, T = _check_pack(zr, ids, mask, pos, R, use_unpad)
+    y = np.random.default_rng(13).standard_normal(ids.shape + (width,)).astype(np.float32)
+    ty = torch.from_numpy(y).to(DEV, dtype)
+    fused = zr.reconstruct_pack_backward(ginfo, ty)
+    two_step = zr.pack_rows_backward(ginfo, zr.reconstruct_backward(ginfo, ty))
+    torch.cuda.synchronize()
+    zr.check_status(ginfo)
+    assert torch.equal(fused, two_step)
+    yv = ty.float().cpu().numpy().astype(np.float64)
+    ref = oracle.pack_rows_backward(oracle.reconstruct_backward(yv, info), info)
+    absum = oracle.pack_rows_backward(oracle.reconstruct_backward(np.abs(yv), info), info)
+    g = fused.float().cpu().numpy().astype(np.float64)
+    tol = 2.0 ** -18 * absum + (2.0 ** -8 * np.abs(ref) if dtype == torch.bfloat16 else 0.0) + 1e-30
+    assert np.all(np.abs(g - ref) <= tol), float(np.max(np.abs(g - ref) - tol))
+
+
+@pytest.mark.parametrize("wname", ["worked_example", "pipeline", "long_context"])
+def test_pack_backward_full_size(zr, wname):
+    """Full-size layouts (padded and, with a mask, unpadded): the pack adjoint
+    bit-exact against the oracle, the fused round trip bitwise equal to the
+    two adjoints in sequence."""
+    wl = WORKLOADS[wname]
+    idx = list(WORKLOADS).index(wname)
+    ids, mask, pos = make_workload_batch(wl, idx)
+    for use_unpad in ([False, True] if mask is not None else [False]):
+        ginfo, info, T = _check_pack(zr, ids, mask, pos, wl.R, use_unpad)
+        _check_pack_backward(zr, ginfo, info, ids.shape, 8, torch.bfloat16, idx)
+        ty = torch.randn(ids.shape + (64,), generator=torch.Generator().manual_seed(idx)).to(DEV, torch.bfloat16)
+        fused = zr.reconstruct_pack_backward(ginfo, ty)
+        two_step = zr.pack_rows_backward(ginfo, zr.reconstruct_backward(ginfo, ty))
+        torch.cuda.synchronize()
+        zr.check_status(ginfo)
+        assert torch.equal(fused, two_step)
