@@ -162,9 +162,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(b_sfull(t), 1);
-            mbar_init(b_pfull(t), 256);
+            mbar_init(b_pfull(t), 8);  // one arrival per softmax warp of head t
             mbar_init(b_odone(t), 1);
-            mbar_init(b_xchg(t), 256);
+            mbar_init(b_xchg(t), 8);
         }
         ring_init(ring, 17);  // the MMA warp and 16 softmax warps
         *abort_flag = 0;
@@ -223,13 +223,14 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     return true;
                 };
                 // the order of pos_k / pos_v
-                for (int w = 0; w < W && ok; ++w) ok = load(&tm_k, ph.hk[w], key_block_row(t, npb, 0));
+                auto hk_of = [&](int w) { return w ? ph.hk[1] : ph.hk[0]; };
+                for (int w = 0; w < W && ok; ++w) ok = load(&tm_k, hk_of(w), key_block_row(t, npb, 0));
                 for (int j = 1; j < n && ok; ++j)
                     for (int w = 0; w < W && ok; ++w) {
-                        ok = load(&tm_k, ph.hk[w], key_block_row(t, npb, j));
-                        if (ok) ok = load(&tm_v, ph.hk[w], key_block_row(t, npb, j - 1));
+                        ok = load(&tm_k, hk_of(w), key_block_row(t, npb, j));
+                        if (ok) ok = load(&tm_v, hk_of(w), key_block_row(t, npb, j - 1));
                     }
-                for (int w = 0; w < W && ok; ++w) ok = load(&tm_v, ph.hk[w], key_block_row(t, npb, n - 1));
+                for (int w = 0; w < W && ok; ++w) ok = load(&tm_v, hk_of(w), key_block_row(t, npb, n - 1));
                 if (!ok) break;
             }
             const long long lim = p.limit;
@@ -253,9 +254,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         };
         constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-        const uint32_t colS[2] = {C::kColS0, C::kColS1};
-        const uint32_t colO[2] = {C::kColO0, C::kColO1};
-        const uint32_t sQ[2] = {sQ0, sQ1};
+        // per-slot addresses as selects (a runtime-indexed array would live in
+        // local memory on the issue path)
+        auto colS = [&](int t) -> uint32_t { return t ? C::kColS1 : C::kColS0; };
+        auto colO = [&](int t) -> uint32_t { return t ? C::kColO1 : C::kColO0; };
+        auto sQ = [&](int t) -> uint32_t { return t ? sQ1 : sQ0; };
         int base = 0, k = 0;
         int pcnt[2] = {0, 0};
         bool ok = true;
@@ -267,11 +270,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         };
         // S_t = Q_t K^T (K in ring slot kslot)
         auto issue_s = [&](int t, int kslot) {
-            const uint64_t dq0 = smem_desc(sQ[t], 16, 1024), dk0 = smem_desc(sKV + kslot * C::kKVBytes, 16, 1024);
+            const uint64_t dq0 = smem_desc(sQ(t), 16, 1024), dk0 = smem_desc(sKV + kslot * C::kKVBytes, 16, 1024);
 #pragma unroll
             for (int s = 0; s < D / 16; ++s) {
                 const uint32_t off = ((s >> 2) * kChunkBytes + (s & 3) * 32) >> 4;
-                if (leader) mma_bf16_ss(tmem + colS[t], dq0 + off, dk0 + off, idesc_s, s > 0 ? 1u : 0u);
+                if (leader) mma_bf16_ss(tmem + colS(t), dq0 + off, dk0 + off, idesc_s, s > 0 ? 1u : 0u);
             }
             if (leader) mma_commit(b_sfull(t));
         };
@@ -284,7 +287,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
             for (int s = 0; s < 8; ++s)
                 if (leader)
-                    mma_bf16_ts(tmem + colO[t], tmem + colS[t] + 8 * s, dv0 + s * 128, idesc_pv,
+                    mma_bf16_ts(tmem + colO(t), tmem + colS(t) + 8 * s, dv0 + s * 128, idesc_pv,
                                 (acc || s > 0) ? 1u : 0u);
             return true;
         };
@@ -360,8 +363,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const float sl2 = p.scale_log2;
         int s_cnt = 0, x_cnt = 0, o_cnt = 0;
         bool ok = true;
+        // one arrival per warp, after every lane's shared-memory write
         auto xwait = [&]() -> bool {
-            mbar_arrive(b_xchg(t));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_xchg(t));
             const bool w = __all_sync(0xffffffffu, mbar_wait(b_xchg(t), x_cnt & 1, ab, 10));
             ++x_cnt;
             return w;
@@ -372,7 +377,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             int ti, hp;
             decode_unit(u, p.group_off, p.B, p.npairs, ti, hp);
             const QTile tile = p.qtiles[ti];
-            const int h = pair_heads(hp, p.Hq, p.ratio).h[t];
+            const PairHeads ph = pair_heads(hp, p.Hq, p.ratio);
+            const int h = t ? ph.h[1] : ph.h[0];
             // slot 1 of the last pair of an odd head count repeats slot 0's head
             const bool own_head = t == 0 || 2 * hp + 1 < p.Hq;
             const int npb = cdiv128(tile.pk1 - tile.pk0);
@@ -450,7 +456,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(b_pfull(t));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_pfull(t));
             }
             if (!ok) break;
             // epilogue: row sums exchanged, O / l for this part's half, the log-sum-exp

@@ -266,9 +266,9 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int h = 0; h < 2; ++h) {
             mbar_init(b_sfull(h), 1);
             mbar_init(b_dpfull(h), 1);
-            mbar_init(b_pdsfull(h), 512);
+            mbar_init(b_pdsfull(h), 16);  // one arrival per softmax warp
             mbar_init(b_dqfull(h), 1);
-            mbar_init(b_dqfree(h), 512);
+            mbar_init(b_dqfree(h), 16);
         }
         ring_init(ring, 17);
         *abort_flag = 0;
@@ -481,7 +481,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tmem_ld16(trow + C::col_p(hf) + 16 * wg, v);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(b_dqfree(hf));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_dqfree(hf));
             const int qlo = 64 * hf + 16 * wg;
             if (r < D && qlo < qb.nq) {
                 float* dst = p.dq_accum + ((int64_t)(qb.q0 + qlo) * p.Hq + h) * D + r;
@@ -587,8 +588,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     fence_async_smem();
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(b_pdsfull(hf));
-                    __syncwarp();  // every lane read `st` before the next half rewrites it
+                    // every lane's TMEM and shared-memory writes (and its reads of
+                    // `st`) precede the warp's one arrival
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_pdsfull(hf));
                     // the other half's dQ^T, issued after this half's GEMMs began
                     if (hf == 0 && it > 0) {
                         if (!readout(1, qb_prev, h_prev)) { ok = false; break; }
