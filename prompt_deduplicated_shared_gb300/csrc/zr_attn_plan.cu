@@ -194,7 +194,7 @@ size_t attn_workspace_layout(const zr_recon_info& info, int Hq, int D, void* bas
     w.delta = static_cast<float*>(take(sizeof(float) * (size_t)info.T_cap * Hq));
     w.delta_t = static_cast<float*>(take(sizeof(float) * (size_t)info.T_cap * Hq));
     w.lse2_t = static_cast<float*>(take(sizeof(float) * (size_t)info.T_cap * Hq));
-    // fp32 dQ accumulator of the tensor-core backward, [T_cap, Hq, D]
+    // fp32 dQ accumulator of the tensor-core backward, [Hq, T_cap, D]
     w.dq_accum = D > 0 ? static_cast<float*>(take(sizeof(float) * (size_t)info.T_cap * Hq * D)) : nullptr;
     w.bytes = off;
     if (ws) *ws = w;

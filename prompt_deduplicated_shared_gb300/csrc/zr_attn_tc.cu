@@ -361,6 +361,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint32_t colS = t ? C::kColS1 : C::kColS0;
         const uint32_t colO = (t ? C::kColO1 : C::kColO0) + (D / 2) * part;  // this part's half of O
         const float sl2 = p.scale_log2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
         int s_cnt = 0, x_cnt = 0, o_cnt = 0;
         bool ok = true;
         // one arrival per warp, after every lane's shared-memory write
@@ -422,35 +423,49 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const bool need = j > 0 && mnew > m + 8.0f;
                 const float alpha = need ? ex2(m - mnew) : 1.0f;
                 if (j == 0 || need) m = mnew;
-                const float mneg = -m;
-                float lp[8];  // row sum as 8 independent partial sums
+                const uint64_t mneg2 = f2_pack(-m, -m);
+                // row sum as 8 independent partial sums, held as four fp32 pairs;
+                // exponent arguments and sums two columns per instruction
+                uint64_t lp2[4];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) lp[q] = 0.f;
+                for (int q = 0; q < 4; ++q) lp2[q] = 0ull;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        const float e0 = ex2(fmaf(__uint_as_float(sr[c][i]), sl2, mneg));
-                        const float e1 = ex2(fmaf(__uint_as_float(sr[c][i + 1]), sl2, mneg));
-                        lp[i & 7] += e0;
-                        lp[(i + 1) & 7] += e1;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), sl2x2,
+                                         mneg2),
+                                  x0, x1);
+                        const float e0 = ex2(x0);
+                        const float e1 = ex2(x1);
+                        lp2[(i & 7) >> 1] = f2_add(lp2[(i & 7) >> 1], f2_pack(e0, e1));
                         pk[i >> 1] = pack_bf16x2(e0, e1);
                     }
                     // P (bf16 pairs) of keys [64 part + 32 c, +32) over S columns already read
                     tmem_st16(trow + colS + 32 * part + 16 * c, pk);
                 }
+                float lp[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) f2_unpack(lp2[q], lp[2 * q], lp[2 * q + 1]);
                 l = l * alpha + (((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7])));
                 // O_t holds P V up to block j - 1: its last MMA completed before S_t(j),
                 // whose completion this thread observed; P V of block j waits for pfull
                 if (__any_sync(0xffffffffu, need)) {
+                    const uint64_t alpha2 = f2_pack(alpha, alpha);
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c) {
                         uint32_t o[32];
                         tmem_ld32(trow + colO + 32 * c, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            float a0, a1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), alpha2), a0, a1);
+                            o[i] = __float_as_uint(a0);
+                            o[i + 1] = __float_as_uint(a1);
+                        }
                         tmem_st32(trow + colO + 32 * c, o);
                     }
                 }

@@ -59,9 +59,22 @@ __device__ __forceinline__ void st_shared_v4_nc(uint32_t addr, uint32_t a, uint3
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
+// the same at a compile-time byte offset from `base` (no address arithmetic)
+template <int kOffBytes>
+__device__ __forceinline__ void red_add_f32_at(float* base, float v) {
+    asm volatile("red.global.add.f32 [%0+%2], %1;" ::"l"(base), "f"(v), "n"(kOffBytes) : "memory");
+}
+// v[j] into base[j * kStride], j = 0..15
+template <int kStride, int J = 0>
+__device__ __forceinline__ void red_add_16(float* base, const uint32_t (&v)[16]) {
+    if constexpr (J < 16) {
+        red_add_f32_at<J * kStride * 4>(base, __uint_as_float(v[J]));
+        red_add_16<kStride, J + 1>(base, v);
+    }
+}
 
 // Delta = rowsum(dO * O) and LSE * log2(e), head-major [Hq, T_cap], rows < T;
-// the fp32 dQ accumulator of those rows is zeroed.
+// the fp32 dQ accumulator ([Hq, T_cap, D], head-major) of those rows is zeroed.
 __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                      const float* __restrict__ lse, const int32_t* __restrict__ total_tokens,
                                      int64_t T_cap, int Hq, int D, float* __restrict__ delta_t,
@@ -84,7 +97,9 @@ __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const 
             s += __uint_as_float(xs[i] << 16) * __uint_as_float(ys[i] << 16);
             s += __uint_as_float(xs[i] & 0xffff0000u) * __uint_as_float(ys[i] & 0xffff0000u);
         }
-        float4* acc = reinterpret_cast<float4*>(dq_accum + row * D) + 2 * part;
+        const int64_t t = row / Hq;
+        const int64_t h = row - t * Hq;
+        float4* acc = reinterpret_cast<float4*>(dq_accum + (h * T_cap + t) * D) + 2 * part;
         acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
         acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -98,14 +113,20 @@ __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const 
     }
 }
 
-// dQ = scale * accumulator, bf16, rows < T; eight values per thread
+// dQ [T, Hq, D] = scale * accumulator [Hq, T_cap, D], bf16, rows < T; eight
+// values per thread (a row of D values is contiguous on both sides)
 __global__ void attn_dq_convert_kernel(const float* __restrict__ dq_accum, const int32_t* __restrict__ total_tokens,
-                                       int64_t T_cap, int64_t row_elems, float scale,
-                                       __nv_bfloat16* __restrict__ dq) {
-    const int64_t n8 = min((int64_t)total_tokens[0], T_cap) * row_elems / 8;
+                                       int64_t T_cap, int Hq, int D, float scale, __nv_bfloat16* __restrict__ dq) {
+    const int d8 = D / 8;
+    const int64_t n8 = min((int64_t)total_tokens[0], T_cap) * Hq * d8;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(dq_accum) + 2 * i);
-        const float4 b = __ldcs(reinterpret_cast<const float4*>(dq_accum) + 2 * i + 1);
+        const int64_t row = i / d8;  // token-major (t, h)
+        const int c = (int)(i - row * d8);
+        const int64_t t = row / Hq;
+        const int64_t h = row - t * Hq;
+        const float4* src = reinterpret_cast<const float4*>(dq_accum + (h * T_cap + t) * D) + 2 * c;
+        const float4 a = __ldcs(src);
+        const float4 b = __ldcs(src + 1);
         uint4 w;
         w.x = pack_bf16x2(a.x * scale, a.y * scale);
         w.y = pack_bf16x2(a.z * scale, a.w * scale);
@@ -127,7 +148,7 @@ struct BwdParams {
     const float* delta_t;
     const float* lse2_t;
     int64_t T_cap;
-    float* dq_accum;   // [T_cap, Hq, D] fp32
+    float* dq_accum;   // [Hq, T_cap, D] fp32: consecutive queries of a head are D floats apart
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     float scale;
@@ -462,14 +483,16 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const float sl2 = p.scale_log2;
         int s_cnt[2] = {0, 0}, dp_cnt[2] = {0, 0}, rd_cnt[2] = {0, 0};
         bool ok = true;
-        // lane < 16: LSE of query column 16 wg + lane of half `hf`; lane >= 16: its Delta
+        // lane < 16: -LSE (base 2) of query column 16 wg + lane of half `hf`;
+        // lane >= 16: its Delta.  Columns past the block's queries get -inf (P = 0).
         auto stage_value = [&](const QBlock& qb, int hf, int hh_, int hk_) -> float {
             const int h = hk_ * p.ratio + hh_;
             const int qc = 64 * hf + 16 * wg + (lane & 15);
-            if (qc >= qb.nq) return lane < 16 ? INFINITY : 0.f;
-            return lane < 16 ? p.lse2_t[(int64_t)h * p.T_cap + qb.q0 + qc]
+            if (qc >= qb.nq) return lane < 16 ? -INFINITY : 0.f;
+            return lane < 16 ? -p.lse2_t[(int64_t)h * p.T_cap + qb.q0 + qc]
                              : p.delta_t[(int64_t)h * p.T_cap + qb.q0 + qc];
         };
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
         // dQ^T of half hf of block qb (query head h): this warpgroup's 16 query
         // columns, added into the fp32 accumulator; lanes are head-dim rows, so
         // a warp's adds for one query cover 32 consecutive floats
@@ -485,12 +508,15 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (lane == 0) mbar_arrive(b_dqfree(hf));
             const int qlo = 64 * hf + 16 * wg;
             if (r < D && qlo < qb.nq) {
-                float* dst = p.dq_accum + ((int64_t)(qb.q0 + qlo) * p.Hq + h) * D + r;
-                const int64_t stride = (int64_t)p.Hq * D;
+                float* dst = p.dq_accum + ((int64_t)h * p.T_cap + qb.q0 + qlo) * D + r;
                 const int nv = qb.nq - qlo;
+                if (nv >= 16) {
+                    red_add_16<D>(dst, v);  // immediate offsets, no per-query arithmetic
+                } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (j < nv) red_add_f32(dst + j * stride, __uint_as_float(v[j]));
+                    for (int j = 0; j < 16; ++j)
+                        if (j < nv) red_add_f32(dst + j * D, __uint_as_float(v[j]));
+                }
             }
             return true;
         };
@@ -537,12 +563,17 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
                         for (int pc = 0; pc < 4; ++pc) {
+                            // S * scale * log2(e) - LSE * log2(e), two columns per instruction
                             const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * pc);
-                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                            float x[4];
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * pc]), __uint_as_float(sr[4 * pc + 1])),
+                                             sl2x2, f2_pack(l4.x, l4.y)), x[0], x[1]);
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * pc + 2]), __uint_as_float(sr[4 * pc + 3])),
+                                             sl2x2, f2_pack(l4.z, l4.w)), x[2], x[3]);
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const int col = 4 * pc + i;
-                                float pr = ex2(fmaf(__uint_as_float(sr[col]), sl2, -lv[i]));
+                                float pr = ex2(x[i]);
                                 if (kMasked) pr = (col >= qlo) ? pr : 0.f;
                                 pv[col] = pr;
                             }
@@ -563,11 +594,17 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     uint32_t pk[8], dk[8];
 #pragma unroll
                     for (int pc = 0; pc < 4; ++pc) {
+                        // dS = P * (dP - Delta), two columns per instruction
                         const float4 d4 = *reinterpret_cast<const float4*>(st + 16 + 4 * pc);
-                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
                         float ds[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) ds[i] = pv[4 * pc + i] * (__uint_as_float(dr[4 * pc + i]) - dv[i]);
+                        f2_unpack(f2_mul(f2_pack(pv[4 * pc], pv[4 * pc + 1]),
+                                         f2_sub(f2_pack(__uint_as_float(dr[4 * pc]), __uint_as_float(dr[4 * pc + 1])),
+                                                f2_pack(d4.x, d4.y))),
+                                  ds[0], ds[1]);
+                        f2_unpack(f2_mul(f2_pack(pv[4 * pc + 2], pv[4 * pc + 3]),
+                                         f2_sub(f2_pack(__uint_as_float(dr[4 * pc + 2]), __uint_as_float(dr[4 * pc + 3])),
+                                                f2_pack(d4.z, d4.w))),
+                                  ds[2], ds[3]);
                         pk[2 * pc] = pack_bf16x2(pv[4 * pc], pv[4 * pc + 1]);
                         pk[2 * pc + 1] = pack_bf16x2(pv[4 * pc + 2], pv[4 * pc + 3]);
                         dk[2 * pc] = pack_bf16x2(ds[0], ds[1]);
@@ -700,9 +737,8 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     }
     {
         KernelTimer timer("attn_dq_convert", s);
-        attn_dq_convert_kernel<<<num_sms() * 8, 256, 0, s>>>(ws.dq_accum, info.total_tokens, a.T_cap,
-                                                             (int64_t)a.Hq * D, a.scale,
-                                                             static_cast<__nv_bfloat16*>(a.dq));
+        attn_dq_convert_kernel<<<num_sms() * 8, 256, 0, s>>>(ws.dq_accum, info.total_tokens, a.T_cap, a.Hq, D,
+                                                             a.scale, static_cast<__nv_bfloat16*>(a.dq));
         ZR_LAUNCH_CHECK("attn_dq_convert_kernel");
     }
     return ZR_OK;

@@ -135,7 +135,7 @@ struct AttnWorkspace {
     float* delta;        // [T_cap, Hq] rowsum(dO * O), backward only (SIMT)
     float* delta_t;      // [Hq, T_cap] rowsum(dO * O), backward only (tensor cores)
     float* lse2_t;       // [Hq, T_cap] log-sum-exp in base 2, backward only (tensor cores)
-    float* dq_accum;     // [T_cap, Hq, D] fp32, tensor-core backward only
+    float* dq_accum;     // [Hq, T_cap, D] fp32, tensor-core backward only
     size_t bytes;
 };
 
