@@ -9,13 +9,14 @@
 // Each of the five GEMMs (S, dP, dV, dK, dQ) runs once per attended block.
 //
 // Three launches:
-//   attn_bwd_prep_kernel     Delta and LSE (base 2) per (head, row),
+//   attn_bwd_prep_kernel     (-LSE * log2(e), Delta) pairs per (head, row),
 //                            head-major, and zeroes the fp32 dQ accumulator
 //   attn_bwd_tc_kernel       key-tile-major: per work unit (key tile, key/value
 //                            head) the K and V tiles stay in shared memory while
 //                            the query blocks that see them (all query heads of
 //                            the group) stream through a TMA ring of 64-query
-//                            halves; per half, S^T = K Q^T and dP^T = V dO^T go
+//                            halves (with the half's block descriptor and its
+//                            LSE/Delta pairs); per half, S^T = K Q^T and dP^T = V dO^T go
 //                            to TMEM, the softmax warps write P^T and dS^T back
 //                            to TMEM (bf16) and dS to shared memory, then
 //                            dV += P^T dO, dK += dS^T Q (A operands from TMEM)
@@ -73,12 +74,14 @@ __device__ __forceinline__ void red_add_16(float* base, const uint32_t (&v)[16])
     }
 }
 
-// Delta = rowsum(dO * O) and LSE * log2(e), head-major [Hq, T_cap], rows < T;
-// the fp32 dQ accumulator ([Hq, T_cap, D], head-major) of those rows is zeroed.
+// Pairs (-LSE * log2(e), Delta = rowsum(dO * O)), head-major [Hq, pitch, 2]:
+// rows < T from the forward, rows [T, T_cap) zero (they are only read for
+// query columns that the backward masks).  The fp32 dQ accumulator ([Hq,
+// T_cap, D], head-major) of rows < T is zeroed.
 __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                      const float* __restrict__ lse, const int32_t* __restrict__ total_tokens,
-                                     int64_t T_cap, int Hq, int D, float* __restrict__ delta_t,
-                                     float* __restrict__ lse2_t, float* __restrict__ dq_accum) {
+                                     int64_t T_cap, int64_t pitch, int Hq, int D, float2* __restrict__ lse_delta,
+                                     float* __restrict__ dq_accum) {
     // one (token, head) row per group of D / 8 lanes, one 16-byte vector of O
     // and of dO per lane
     const int G = D >> 3;
@@ -105,11 +108,10 @@ __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const 
     }
     // reduce over the row's lanes (groups of G consecutive lanes, G a power of two)
     for (int off = G >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (valid && part == 0) {
+    if (part == 0 && row < T_cap * Hq) {
         const int64_t t = row / Hq;
         const int h = (int)(row - t * Hq);
-        delta_t[(int64_t)h * T_cap + t] = s;
-        lse2_t[(int64_t)h * T_cap + t] = lse[row] * kLog2e;
+        lse_delta[(int64_t)h * pitch + t] = valid ? make_float2(-lse[row] * kLog2e, s) : make_float2(0.f, 0.f);
     }
 }
 
@@ -145,8 +147,6 @@ struct BwdParams {
     const int2* rblocks;
     int B;
     int Hq, Hkv, ratio;
-    const float* delta_t;
-    const float* lse2_t;
     int64_t T_cap;
     float* dq_accum;   // [Hq, T_cap, D] fp32: consecutive queries of a head are D floats apart
     __nv_bfloat16* dk;
@@ -175,9 +175,17 @@ struct BwdCfg {
     // dqfull[2], dqfree[2], unit ring (4), mma drain
     static constexpr int kNumBars = 2 + 2 * kStages + 10 + 4 + 1;
     static constexpr int kDataBytes = 2 * kTile + kStages * 2 * kHalf + 2 * kDS;
-    // data, LSE/Delta staging (2 KB), barriers, misc words; the dynamic shared
-    // memory base is 1024-aligned (checked at run time)
-    static constexpr int kSmemBytes = kDataBytes + 2048 + kNumBars * 8 + 64;
+    // per half-slot, beside Q and dO: the (-LSE * log2(e), Delta) pairs of 68
+    // rows from the half's first row rounded down to a multiple of 4 (one TMA
+    // box: its x coordinate must be 16-byte aligned), and the half's block
+    // descriptor {q0, nq, query head, diagonal}
+    static constexpr int kLdRows = 68;
+    static constexpr int kLdBytes = kLdRows * 8;
+    static constexpr int kLdStride = 640;  // 128-byte aligned slot areas
+    static constexpr int kMetaBytes = 16;
+    // data, LSE/Delta slots, descriptors, barriers, misc words; the dynamic
+    // shared memory base is 1024-aligned (checked at run time)
+    static constexpr int kSmemBytes = kDataBytes + kStages * (kLdStride + kMetaBytes) + kNumBars * 8 + 64;
     // TMEM: dV [0, D), dK [D, 2D); query half h: S^T [2D + 128h, +64) and
     // dP^T [2D + 128h + 64, +64).  The softmax writes P^T and dS^T (bf16 pairs)
     // back over the S^T columns it read; dQ^T of the half (fp32, lanes = head
@@ -247,7 +255,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const BwdParams p) {
+                   const __grid_constant__ CUtensorMap tm_ld, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t s0 = smem_u32(smem);
@@ -258,8 +266,9 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t sK = s0, sV = s0 + C::kTile;
     const uint32_t sQD = s0 + 2 * C::kTile;  // half-slot s: Q_h at sQD + s*2*kHalf, dO_h at + kHalf
     const uint32_t sDS = sQD + C::kStages * 2 * C::kHalf;  // half h at sDS + h*kDS
-    float* stage_f = reinterpret_cast<float*>(smem + C::kDataBytes);  // [16 warps][32]: 16 LSE, 16 Delta
-    const uint32_t bar0 = s0 + C::kDataBytes + 2048;
+    const uint32_t sLD = s0 + C::kDataBytes;                   // slot s: pairs at sLD + s*kLdStride
+    const uint32_t sMeta = sLD + C::kStages * C::kLdStride;    // slot s: int4 at sMeta + 16 s
+    const uint32_t bar0 = sMeta + C::kStages * C::kMetaBytes;
     const uint32_t b_kfull = bar0, b_kempty = bar0 + 8;
     auto b_qfull = [&](int s) { return bar0 + 16 + 8 * s; };
     auto b_qempty = [&](int s) { return bar0 + 16 + 8 * (C::kStages + s); };
@@ -269,7 +278,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     auto b_pdsfull = [&](int h) { return b_rest + 32 + 8 * h; };
     auto b_dqfull = [&](int h) { return b_rest + 48 + 8 * h; };
     auto b_dqfree = [&](int h) { return b_rest + 64 + 8 * h; };
-    uint8_t* misc = smem + C::kDataBytes + 2048 + C::kNumBars * 8;
+    uint8_t* misc = smem + (bar0 - s0) + C::kNumBars * 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8);
     const UnitRing ring{b_rest + 80, b_rest + 96, reinterpret_cast<volatile int*>(misc + 16)};
@@ -312,6 +321,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
+            prefetch_tmap(&tm_ld);
             int qstage = 0, k = 0, last_k = -1;
             bool ok = true;
             for (; ok; ++k) {
@@ -340,9 +350,14 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         for (int half = 0; half < 2; ++half) {
                             const int slot = qstage % C::kStages, r = qstage / C::kStages;
                             if (r > 0 && !mbar_wait(b_qempty(slot), (r - 1) & 1, ab, 32)) { ok = false; break; }
-                            mbar_expect_tx(b_qfull(slot), 2 * C::kHalf);
-                            const uint32_t qb_s = sQD + slot * 2 * C::kHalf;
                             const int row = qb.q0 + 64 * half;
+                            // the descriptor precedes the arrival (release) that the
+                            // consumers acquire through the same barrier
+                            st_shared_v4_nc(sMeta + slot * C::kMetaBytes, (uint32_t)qb.q0, (uint32_t)qb.nq,
+                                            (uint32_t)h, qb.diag ? 1u : 0u);
+                            mbar_expect_tx(b_qfull(slot), 2 * C::kHalf + C::kLdBytes);
+                            tma_load_2d(sLD + slot * C::kLdStride, &tm_ld, 2 * (row & ~3), h, b_qfull(slot));
+                            const uint32_t qb_s = sQD + slot * 2 * C::kHalf;
 #pragma unroll
                             for (int c = 0; c < C::kChunks; ++c) {
                                 tma_load_2d(qb_s + c * C::kHalfChunk, &tm_q, h * D + 64 * c, row, b_qfull(slot));
@@ -475,23 +490,16 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // softmax warps: warpgroup wg owns query columns [16 wg, +16) of each
         // 64-query half; all four warpgroups take half A, then half B.  TMEM
         // lane r is key row r of S^T / dP^T and head-dimension row r of dQ^T.
+        // The query block, its head and its LSE/Delta come from the half-slot
+        // (written by the producer), so the loop reads no global memory.
         const int wg = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-        float* st = stage_f + (warp - 2) * 32;  // this warp's 16 LSE (base 2) then 16 Delta
         const float sl2 = p.scale_log2;
         int s_cnt[2] = {0, 0}, dp_cnt[2] = {0, 0}, rd_cnt[2] = {0, 0};
+        int qstage = 0;  // half-slot sequence, as the producer and the MMA warp run it
         bool ok = true;
-        // lane < 16: -LSE (base 2) of query column 16 wg + lane of half `hf`;
-        // lane >= 16: its Delta.  Columns past the block's queries get -inf (P = 0).
-        auto stage_value = [&](const QBlock& qb, int hf, int hh_, int hk_) -> float {
-            const int h = hk_ * p.ratio + hh_;
-            const int qc = 64 * hf + 16 * wg + (lane & 15);
-            if (qc >= qb.nq) return lane < 16 ? -INFINITY : 0.f;
-            return lane < 16 ? -p.lse2_t[(int64_t)h * p.T_cap + qb.q0 + qc]
-                             : p.delta_t[(int64_t)h * p.T_cap + qb.q0 + qc];
-        };
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         // dQ^T of half hf of block qb (query head h): this warpgroup's 16 query
         // columns, added into the fp32 accumulator; lanes are head-dim rows, so
@@ -529,22 +537,16 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const int key_pos = t.k0 + r;
             const bool key_ok = r < t.nk;  // rows past the tile's keys give no dS (they feed dQ)
             const int iters = t.nqblk * p.ratio;
-            const int rb_base = t.kind == 0 ? p.kgroup_off[t.g] : 0;
-            QBlock qb_next = qblock_of(t, p, 0, rb_base);
-            QBlock qb_prev = qb_next;
+            QBlock qb_prev{0, 0, false};
             int h_prev = 0;
-            float pre_next = stage_value(qb_next, 0, 0, hk);
             for (int it = 0; it < iters && ok; ++it) {
-                const QBlock qb = qb_next;
-                const int h_cur = hk * p.ratio + it / t.nqblk;
-                if (it + 1 < iters) qb_next = qblock_of(t, p, (it + 1) % t.nqblk, rb_base);
+                QBlock qb{0, 0, false};
+                int h_cur = 0;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const float pre = pre_next;
-                    // the value staged for the next half, loaded before this half's
-                    // S^T is awaited so that its latency hides behind the wait
-                    if (hf == 0) pre_next = stage_value(qb, 1, it / t.nqblk, hk);
-                    else if (it + 1 < iters) pre_next = stage_value(qb_next, 0, (it + 1) / t.nqblk, hk);
+                    const int slot = qstage % C::kStages;
+                    const uint32_t qph = (uint32_t)(qstage / C::kStages) & 1u;
+                    ++qstage;
                     if (!__all_sync(0xffffffffu, mbar_wait(b_sfull(hf), s_cnt[hf] & 1, ab, 36))) {
                         ok = false;
                         break;
@@ -553,33 +555,47 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     tc_fence_after();
                     uint32_t sr[16];
                     tmem_ld16(trow + C::col_s(hf) + 16 * wg, sr);
-                    st[lane] = pre;
-                    __syncwarp();
+                    // the slot was filled before S^T was issued; this wait completes
+                    // at once and makes the producer's descriptor and pairs visible
+                    if (!__all_sync(0xffffffffu, mbar_wait(b_qfull(slot), qph, ab, 41))) {
+                        ok = false;
+                        break;
+                    }
+                    if (hf == 0) {
+                        const int4 m = *reinterpret_cast<const int4*>(smem + (sMeta - s0) + slot * C::kMetaBytes);
+                        qb.q0 = m.x;
+                        qb.nq = m.y;
+                        h_cur = m.z;
+                        qb.diag = m.w != 0;
+                    }
+                    const int row0 = qb.q0 + 64 * hf;
+                    // pairs (-LSE * log2(e), Delta) of this warpgroup's 16 query columns
+                    const float2* ldv = reinterpret_cast<const float2*>(smem + (sLD - s0) + slot * C::kLdStride) +
+                                        (row0 & 3) + 16 * wg;
+                    const int nv = qb.nq - 64 * hf - 16 * wg;  // valid query columns of this warpgroup
                     tmem_wait_ld();
                     // P^T from S^T and the staged LSE
-                    const int qlo = key_ok ? key_pos - qb.q0 - 64 * hf - 16 * wg : (1 << 30);  // causal: query >= key
+                    const int qlo = key_ok ? key_pos - row0 - 16 * wg : (1 << 30);  // causal: query >= key
                     float pv[16];
                     auto probs = [&](auto masked) {
                         constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
-                        for (int pc = 0; pc < 4; ++pc) {
+                        for (int pc = 0; pc < 8; ++pc) {
                             // S * scale * log2(e) - LSE * log2(e), two columns per instruction
-                            const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * pc);
-                            float x[4];
-                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * pc]), __uint_as_float(sr[4 * pc + 1])),
-                                             sl2x2, f2_pack(l4.x, l4.y)), x[0], x[1]);
-                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * pc + 2]), __uint_as_float(sr[4 * pc + 3])),
-                                             sl2x2, f2_pack(l4.z, l4.w)), x[2], x[3]);
+                            const float2 a = ldv[2 * pc], b = ldv[2 * pc + 1];
+                            float x[2];
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * pc]), __uint_as_float(sr[2 * pc + 1])),
+                                             sl2x2, f2_pack(a.x, b.x)), x[0], x[1]);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int col = 4 * pc + i;
+                            for (int i = 0; i < 2; ++i) {
+                                const int col = 2 * pc + i;
                                 float pr = ex2(x[i]);
-                                if (kMasked) pr = (col >= qlo) ? pr : 0.f;
+                                if (kMasked) pr = (col >= qlo && col < nv) ? pr : 0.f;
                                 pv[col] = pr;
                             }
                         }
                     };
-                    if (qb.diag || !key_ok) probs(std::integral_constant<bool, true>());
+                    if (qb.diag || !key_ok || nv < 16) probs(std::integral_constant<bool, true>());
                     else probs(std::integral_constant<bool, false>());
                     // dS^T from dP^T and the staged Delta
                     if (!__all_sync(0xffffffffu, mbar_wait(b_dpfull(hf), dp_cnt[hf] & 1, ab, 38))) {
@@ -593,22 +609,17 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     tmem_wait_ld();
                     uint32_t pk[8], dk[8];
 #pragma unroll
-                    for (int pc = 0; pc < 4; ++pc) {
-                        // dS = P * (dP - Delta), two columns per instruction
-                        const float4 d4 = *reinterpret_cast<const float4*>(st + 16 + 4 * pc);
-                        float ds[4];
-                        f2_unpack(f2_mul(f2_pack(pv[4 * pc], pv[4 * pc + 1]),
-                                         f2_sub(f2_pack(__uint_as_float(dr[4 * pc]), __uint_as_float(dr[4 * pc + 1])),
-                                                f2_pack(d4.x, d4.y))),
+                    for (int pc = 0; pc < 8; ++pc) {
+                        // dS = P * (dP - Delta), two columns per instruction (the
+                        // staged Delta of a masked column is finite, so its dS is 0)
+                        const float2 a = ldv[2 * pc], b = ldv[2 * pc + 1];
+                        float ds[2];
+                        f2_unpack(f2_mul(f2_pack(pv[2 * pc], pv[2 * pc + 1]),
+                                         f2_sub(f2_pack(__uint_as_float(dr[2 * pc]), __uint_as_float(dr[2 * pc + 1])),
+                                                f2_pack(a.y, b.y))),
                                   ds[0], ds[1]);
-                        f2_unpack(f2_mul(f2_pack(pv[4 * pc + 2], pv[4 * pc + 3]),
-                                         f2_sub(f2_pack(__uint_as_float(dr[4 * pc + 2]), __uint_as_float(dr[4 * pc + 3])),
-                                                f2_pack(d4.z, d4.w))),
-                                  ds[2], ds[3]);
-                        pk[2 * pc] = pack_bf16x2(pv[4 * pc], pv[4 * pc + 1]);
-                        pk[2 * pc + 1] = pack_bf16x2(pv[4 * pc + 2], pv[4 * pc + 3]);
-                        dk[2 * pc] = pack_bf16x2(ds[0], ds[1]);
-                        dk[2 * pc + 1] = pack_bf16x2(ds[2], ds[3]);
+                        pk[pc] = pack_bf16x2(pv[2 * pc], pv[2 * pc + 1]);
+                        dk[pc] = pack_bf16x2(ds[0], ds[1]);
                     }
                     // P^T and dS^T (bf16 pairs) over the 16 S^T columns read
                     tmem_st8(trow + C::col_s(hf) + 16 * wg, pk);
@@ -626,7 +637,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     tmem_wait_st();
                     tc_fence_before();
                     // every lane's TMEM and shared-memory writes (and its reads of
-                    // `st`) precede the warp's one arrival
+                    // the slot) precede the warp's one arrival
                     __syncwarp();
                     if (lane == 0) mbar_arrive(b_pdsfull(hf));
                     // the other half's dQ^T, issued after this half's GEMMs began
@@ -687,7 +698,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 template <int D>
 zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const AttnArgs& a, cudaStream_t s) {
     using C = BwdCfg<D>;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tld;
     zr_status st;
     // Q and dO: 64-row boxes (the kernel stages them per 64-query half)
     if ((st = make_map(&tq, a.q, (int64_t)a.Hq * D, a.T_cap, (int64_t)a.Hq * D * 2, 64)) != ZR_OK) return st;
@@ -697,12 +708,26 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     if (((uintptr_t)a.dq & 15) || ((uintptr_t)ws.dq_accum & 15))
         return set_error(ZR_ERR_INVALID_ARG, "dq must be 16-byte aligned");
     {
+        // (LSE, Delta) pairs: fp32 [Hq rows, 2 * T_cap columns], row stride
+        // 8 * pitch bytes; boxes of kLdRows pairs, no swizzle, zero fill past T_cap
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return set_error(ZR_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+        cuuint64_t dims[2] = {(cuuint64_t)(2 * a.T_cap), (cuuint64_t)a.Hq};
+        cuuint64_t strides[1] = {(cuuint64_t)(8 * lse_delta_pitch(a.T_cap))};
+        cuuint32_t box[2] = {(cuuint32_t)(2 * C::kLdRows), 1};
+        cuuint32_t estr[2] = {1, 1};
+        const CUresult r = fn(&tld, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws.lse_delta, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return set_error(ZR_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
+    {
         const int64_t threads = a.T_cap * a.Hq * (D / 8);
         const int64_t blocks = (threads + 255) / 256;
         KernelTimer timer("attn_bwd_prep", s);
         attn_bwd_prep_kernel<<<(unsigned)blocks, 256, 0, s>>>(
             static_cast<const __nv_bfloat16*>(a.o_in), static_cast<const __nv_bfloat16*>(a.dout), a.lse_in,
-            info.total_tokens, a.T_cap, a.Hq, D, ws.delta_t, ws.lse2_t, ws.dq_accum);
+            info.total_tokens, a.T_cap, lse_delta_pitch(a.T_cap), a.Hq, D, ws.lse_delta, ws.dq_accum);
         ZR_LAUNCH_CHECK("attn_bwd_prep_kernel");
     }
     BwdParams p;
@@ -716,8 +741,6 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.ratio = a.Hq / a.Hkv;
-    p.delta_t = ws.delta_t;
-    p.lse2_t = ws.lse2_t;
     p.T_cap = a.T_cap;
     p.dq_accum = ws.dq_accum;
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
@@ -732,7 +755,7 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
                                      C::kSmemBytes));
     {
         KernelTimer timer("attn_bwd", s);
-        attn_bwd_tc_kernel<D><<<num_sms(), kBwdThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p);
+        attn_bwd_tc_kernel<D><<<num_sms(), kBwdThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tld, p);
         ZR_LAUNCH_CHECK("attn_bwd_tc_kernel");
     }
     {

@@ -129,12 +129,18 @@ struct AttnPlan {
     int max_qtiles, max_ktiles;
 };
 
+// rows per head of the backward's (LSE, Delta) pairs: T_cap rounded up to a
+// multiple of 4, so that a head's rows start 32-byte aligned (a TMA row stride
+// must be a multiple of 16 bytes)
+inline int64_t lse_delta_pitch(int64_t T_cap) { return (T_cap + 3) & ~(int64_t)3; }
+
 struct AttnWorkspace {
     AttnPlan plan;
     int* status;         // [4] device status words
     float* delta;        // [T_cap, Hq] rowsum(dO * O), backward only (SIMT)
-    float* delta_t;      // [Hq, T_cap] rowsum(dO * O), backward only (tensor cores)
-    float* lse2_t;       // [Hq, T_cap] log-sum-exp in base 2, backward only (tensor cores)
+    // [Hq, lse_delta_pitch(T_cap)] pairs (-LSE * log2(e), rowsum(dO * O)),
+    // backward only (tensor cores)
+    float2* lse_delta;
     float* dq_accum;     // [Hq, T_cap, D] fp32, tensor-core backward only
     size_t bytes;
 };
