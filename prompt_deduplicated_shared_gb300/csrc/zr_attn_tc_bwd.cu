@@ -56,6 +56,10 @@ __device__ __forceinline__ void st_shared_v4_nc(uint32_t addr, uint32_t a, uint3
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
 // fire-and-forget fp32 add in global memory (performed at L2)
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
@@ -148,6 +152,8 @@ struct BwdParams {
     int B;
     int Hq, Hkv, ratio;
     int64_t T_cap;
+    const float2* lse_delta;  // [Hq, ld_pitch] (-LSE * log2(e), Delta)
+    int64_t ld_pitch;
     float* dq_accum;   // [Hq, T_cap, D] fp32: consecutive queries of a head are D floats apart
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
@@ -175,13 +181,11 @@ struct BwdCfg {
     // dqfull[2], dqfree[2], unit ring (4), mma drain
     static constexpr int kNumBars = 2 + 2 * kStages + 10 + 4 + 1;
     static constexpr int kDataBytes = 2 * kTile + kStages * 2 * kHalf + 2 * kDS;
-    // per half-slot, beside Q and dO: the (-LSE * log2(e), Delta) pairs of 68
-    // rows from the half's first row rounded down to a multiple of 4 (one TMA
-    // box: its x coordinate must be 16-byte aligned), and the half's block
-    // descriptor {q0, nq, query head, diagonal}
-    static constexpr int kLdRows = 68;
-    static constexpr int kLdBytes = kLdRows * 8;
-    static constexpr int kLdStride = 640;  // 128-byte aligned slot areas
+    // per half-slot, beside Q and dO: the half's -LSE * log2(e) and Delta as
+    // four 16-query chunks of 128 bytes (16 -LSE values, then 16 Delta
+    // values), so that a softmax warp reads its chunk with 16-byte broadcast
+    // loads, and the half's block descriptor {q0, nq, query head, diagonal}
+    static constexpr int kLdStride = 512;
     static constexpr int kMetaBytes = 16;
     // data, LSE/Delta slots, descriptors, barriers, misc words; the dynamic
     // shared memory base is 1024-aligned (checked at run time)
@@ -255,7 +259,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const __grid_constant__ CUtensorMap tm_ld, const BwdParams p) {
+                   const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t s0 = smem_u32(smem);
@@ -266,7 +270,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t sK = s0, sV = s0 + C::kTile;
     const uint32_t sQD = s0 + 2 * C::kTile;  // half-slot s: Q_h at sQD + s*2*kHalf, dO_h at + kHalf
     const uint32_t sDS = sQD + C::kStages * 2 * C::kHalf;  // half h at sDS + h*kDS
-    const uint32_t sLD = s0 + C::kDataBytes;                   // slot s: pairs at sLD + s*kLdStride
+    const uint32_t sLD = s0 + C::kDataBytes;                   // slot s: chunks at sLD + s*kLdStride
     const uint32_t sMeta = sLD + C::kStages * C::kLdStride;    // slot s: int4 at sMeta + 16 s
     const uint32_t bar0 = sMeta + C::kStages * C::kMetaBytes;
     const uint32_t b_kfull = bar0, b_kempty = bar0 + 8;
@@ -316,47 +320,70 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int n_units = p.counts[1] * p.Hkv;
 
     if (warp == 0) {
+        // producer: the whole warp runs the loop (warp-uniform control); lane 0
+        // takes the units and issues the copies, and every lane stages two
+        // query columns of a half's -LSE/Delta chunks (lane l: chunk l / 8,
+        // columns 2 (l % 8) and 2 (l % 8) + 1)
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
-            prefetch_tmap(&tm_ld);
-            int qstage = 0, k = 0, last_k = -1;
-            bool ok = true;
-            for (; ok; ++k) {
-                const int u = ring_publish(ring, k, p.sched, n_units, ab);
-                if (u < 0) { ok = (u == -1); break; }
-                int ti, hk;
-                decode_unit(u, p.kgroup_off, p.B, p.Hkv, ti, hk);
-                const KTile t = p.ktiles[ti];
-                if (k > 0 && !mbar_wait(b_kempty, (k - 1) & 1, ab, 31)) { ok = false; break; }
-                // test option: the CTA that takes unit 0 withholds its K/V load, so
-                // that a bounded wait runs out and the abort path runs
-                if (!(p.withhold && u == 0)) {
+        }
+        const int lcol = 16 * (lane >> 3) + 2 * (lane & 7);
+        const uint32_t lofs = 128 * (lane >> 3) + 8 * (lane & 7);
+        int qstage = 0, k = 0, last_k = -1;
+        bool ok = true;
+        for (; ok; ++k) {
+            int u = 0;
+            if (lane == 0) u = ring_publish(ring, k, p.sched, n_units, ab);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (u < 0) { ok = (u == -1); break; }
+            int ti, hk;
+            decode_unit(u, p.kgroup_off, p.B, p.Hkv, ti, hk);
+            const KTile t = p.ktiles[ti];
+            if (k > 0 && !__all_sync(0xffffffffu, mbar_wait(b_kempty, (k - 1) & 1, ab, 31))) { ok = false; break; }
+            // test option: the CTA that takes unit 0 withholds its K/V load, so
+            // that a bounded wait runs out and the abort path runs
+            if (!(p.withhold && u == 0)) {
+                if (lane == 0) {
                     mbar_expect_tx(b_kfull, 2 * C::kTile);
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c) {
                         tma_load_2d(sK + c * kChunkBytes, &tm_k, hk * D + 64 * c, t.k0, b_kfull);
                         tma_load_2d(sV + c * kChunkBytes, &tm_v, hk * D + 64 * c, t.k0, b_kfull);
                     }
-                    last_k = k;
                 }
-                const int rb_base = t.kind == 0 ? p.kgroup_off[t.g] : 0;
-                for (int hh = 0; hh < p.ratio && ok; ++hh) {
-                    const int h = hk * p.ratio + hh;
-                    for (int qi = 0; qi < t.nqblk && ok; ++qi) {
-                        const QBlock qb = qblock_of(t, p, qi, rb_base);
-                        for (int half = 0; half < 2; ++half) {
-                            const int slot = qstage % C::kStages, r = qstage / C::kStages;
-                            if (r > 0 && !mbar_wait(b_qempty(slot), (r - 1) & 1, ab, 32)) { ok = false; break; }
-                            const int row = qb.q0 + 64 * half;
-                            // the descriptor precedes the arrival (release) that the
-                            // consumers acquire through the same barrier
+                last_k = k;
+            }
+            const int rb_base = t.kind == 0 ? p.kgroup_off[t.g] : 0;
+            for (int hh = 0; hh < p.ratio && ok; ++hh) {
+                const int h = hk * p.ratio + hh;
+                const float2* ld_h = p.lse_delta + (int64_t)h * p.ld_pitch;
+                for (int qi = 0; qi < t.nqblk && ok; ++qi) {
+                    const QBlock qb = qblock_of(t, p, qi, rb_base);
+                    for (int half = 0; half < 2; ++half) {
+                        const int slot = qstage % C::kStages, r = qstage / C::kStages;
+                        if (r > 0 && !__all_sync(0xffffffffu, mbar_wait(b_qempty(slot), (r - 1) & 1, ab, 32))) {
+                            ok = false;
+                            break;
+                        }
+                        const int row = qb.q0 + 64 * half;
+                        // this lane's two columns (rows past T_cap: zero; the softmax
+                        // masks every column past the block's queries)
+                        const int c0 = row + lcol;
+                        const float2 va = c0 < p.T_cap ? ld_h[c0] : make_float2(0.f, 0.f);
+                        const float2 vb = c0 + 1 < p.T_cap ? ld_h[c0 + 1] : make_float2(0.f, 0.f);
+                        const uint32_t dst = sLD + slot * C::kLdStride + lofs;
+                        st_shared_v2(dst, va.x, vb.x);
+                        st_shared_v2(dst + 64, va.y, vb.y);
+                        // the lanes' stores, then lane 0's descriptor, precede its
+                        // arrival (release) that the consumers acquire
+                        __syncwarp();
+                        if (lane == 0) {
                             st_shared_v4_nc(sMeta + slot * C::kMetaBytes, (uint32_t)qb.q0, (uint32_t)qb.nq,
                                             (uint32_t)h, qb.diag ? 1u : 0u);
-                            mbar_expect_tx(b_qfull(slot), 2 * C::kHalf + C::kLdBytes);
-                            tma_load_2d(sLD + slot * C::kLdStride, &tm_ld, 2 * (row & ~3), h, b_qfull(slot));
+                            mbar_expect_tx(b_qfull(slot), 2 * C::kHalf);
                             const uint32_t qb_s = sQD + slot * 2 * C::kHalf;
 #pragma unroll
                             for (int c = 0; c < C::kChunks; ++c) {
@@ -364,11 +391,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                 tma_load_2d(qb_s + C::kHalf + c * C::kHalfChunk, &tm_do, h * D + 64 * c, row,
                                             b_qfull(slot));
                             }
-                            ++qstage;
                         }
+                        ++qstage;
                     }
                 }
             }
+        }
+        if (lane == 0) {
             const long long lim = p.limit;
             if (ok) {
                 // every load consumed and every release committed before exit
@@ -569,9 +598,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         qb.diag = m.w != 0;
                     }
                     const int row0 = qb.q0 + 64 * hf;
-                    // pairs (-LSE * log2(e), Delta) of this warpgroup's 16 query columns
-                    const float2* ldv = reinterpret_cast<const float2*>(smem + (sLD - s0) + slot * C::kLdStride) +
-                                        (row0 & 3) + 16 * wg;
+                    // -LSE * log2(e) (16 floats), then Delta (16 floats), of this
+                    // warpgroup's 16 query columns
+                    const float4* ldc =
+                        reinterpret_cast<const float4*>(smem + (sLD - s0) + slot * C::kLdStride + 128 * wg);
                     const int nv = qb.nq - 64 * hf - 16 * wg;  // valid query columns of this warpgroup
                     tmem_wait_ld();
                     // P^T from S^T and the staged LSE
@@ -582,10 +612,11 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
                         for (int pc = 0; pc < 8; ++pc) {
                             // S * scale * log2(e) - LSE * log2(e), two columns per instruction
-                            const float2 a = ldv[2 * pc], b = ldv[2 * pc + 1];
+                            const float4 l4 = ldc[pc >> 1];
                             float x[2];
                             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * pc]), __uint_as_float(sr[2 * pc + 1])),
-                                             sl2x2, f2_pack(a.x, b.x)), x[0], x[1]);
+                                             sl2x2, (pc & 1) ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y)),
+                                      x[0], x[1]);
 #pragma unroll
                             for (int i = 0; i < 2; ++i) {
                                 const int col = 2 * pc + i;
@@ -612,11 +643,11 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     for (int pc = 0; pc < 8; ++pc) {
                         // dS = P * (dP - Delta), two columns per instruction (the
                         // staged Delta of a masked column is finite, so its dS is 0)
-                        const float2 a = ldv[2 * pc], b = ldv[2 * pc + 1];
+                        const float4 d4 = ldc[4 + (pc >> 1)];
                         float ds[2];
                         f2_unpack(f2_mul(f2_pack(pv[2 * pc], pv[2 * pc + 1]),
                                          f2_sub(f2_pack(__uint_as_float(dr[2 * pc]), __uint_as_float(dr[2 * pc + 1])),
-                                                f2_pack(a.y, b.y))),
+                                                (pc & 1) ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y))),
                                   ds[0], ds[1]);
                         pk[pc] = pack_bf16x2(pv[2 * pc], pv[2 * pc + 1]);
                         dk[pc] = pack_bf16x2(ds[0], ds[1]);
@@ -698,7 +729,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 template <int D>
 zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const AttnArgs& a, cudaStream_t s) {
     using C = BwdCfg<D>;
-    CUtensorMap tq, tk, tv, tdo, tld;
+    CUtensorMap tq, tk, tv, tdo;
     zr_status st;
     // Q and dO: 64-row boxes (the kernel stages them per 64-query half)
     if ((st = make_map(&tq, a.q, (int64_t)a.Hq * D, a.T_cap, (int64_t)a.Hq * D * 2, 64)) != ZR_OK) return st;
@@ -707,20 +738,6 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     if ((st = make_map(&tv, a.v, (int64_t)a.Hkv * D, a.T_cap, (int64_t)a.Hkv * D * 2)) != ZR_OK) return st;
     if (((uintptr_t)a.dq & 15) || ((uintptr_t)ws.dq_accum & 15))
         return set_error(ZR_ERR_INVALID_ARG, "dq must be 16-byte aligned");
-    {
-        // (LSE, Delta) pairs: fp32 [Hq rows, 2 * T_cap columns], row stride
-        // 8 * pitch bytes; boxes of kLdRows pairs, no swizzle, zero fill past T_cap
-        EncodeTiledFn fn = encode_fn();
-        if (!fn) return set_error(ZR_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-        cuuint64_t dims[2] = {(cuuint64_t)(2 * a.T_cap), (cuuint64_t)a.Hq};
-        cuuint64_t strides[1] = {(cuuint64_t)(8 * lse_delta_pitch(a.T_cap))};
-        cuuint32_t box[2] = {(cuuint32_t)(2 * C::kLdRows), 1};
-        cuuint32_t estr[2] = {1, 1};
-        const CUresult r = fn(&tld, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws.lse_delta, dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return set_error(ZR_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    }
     {
         const int64_t threads = a.T_cap * a.Hq * (D / 8);
         const int64_t blocks = (threads + 255) / 256;
@@ -742,6 +759,8 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     p.Hkv = a.Hkv;
     p.ratio = a.Hq / a.Hkv;
     p.T_cap = a.T_cap;
+    p.lse_delta = ws.lse_delta;
+    p.ld_pitch = lse_delta_pitch(a.T_cap);
     p.dq_accum = ws.dq_accum;
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
@@ -755,7 +774,7 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
                                      C::kSmemBytes));
     {
         KernelTimer timer("attn_bwd", s);
-        attn_bwd_tc_kernel<D><<<num_sms(), kBwdThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, tld, p);
+        attn_bwd_tc_kernel<D><<<num_sms(), kBwdThreads, C::kSmemBytes, s>>>(tq, tk, tv, tdo, p);
         ZR_LAUNCH_CHECK("attn_bwd_tc_kernel");
     }
     {
