@@ -61,6 +61,15 @@ const char* zr_last_error(void);
 /* ABI version of this header (major * 100 + minor). */
 int zr_version(void);
 
+/* 1 in the debug build (libzr_debug.so, compiled with ZR_DEBUG_BOUNDS), else
+ * 0.  The debug build checks every global row index that a kernel derives
+ * from the device-built plans (pack and reconstruction segments, attention
+ * query blocks and key tiles) before the access; a failed check skips the
+ * access and records its site in the reconstruction info's status words,
+ * which zr_check_status reports as ZR_ERR_INVALID_ARG ("debug bounds check
+ * failed at site N").  Same ABI and results as libzr.so otherwise. */
+int zr_debug_bounds(void);
+
 /* Number of kernels this library has launched in this process (all devices),
  * for launch accounting in benchmarks. */
 int64_t zr_kernel_launches(void);

@@ -126,6 +126,14 @@ const char* zr_last_error(void) { return g_msg; }
 
 int zr_version(void) { return 100; }
 
+int zr_debug_bounds(void) {
+#ifdef ZR_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 int64_t zr_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 zr_status zr_set_option(const char* name, int64_t value) {
@@ -504,6 +512,8 @@ zr_status zr_check_status(const zr_recon_info* info, void* attn_workspace, void*
     if (hs[kStatusCapacity]) return set_error(ZR_ERR_CAPACITY, "packed tokens exceed T_cap");
     if (hs[kStatusTimeout])
         return set_error(ZR_ERR_TIMEOUT, "a bounded device wait gave up (code %d)", hs[kStatusTimeout]);
+    if (hs[kStatusBounds])
+        return set_error(ZR_ERR_INVALID_ARG, "debug bounds check failed at site %d", hs[kStatusBounds]);
     if (ha[kStatusTimeout])
         return set_error(ZR_ERR_TIMEOUT, "a bounded device wait gave up (code %d)", ha[kStatusTimeout]);
     return ZR_OK;

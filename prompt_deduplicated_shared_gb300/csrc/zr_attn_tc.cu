@@ -88,6 +88,7 @@ struct FwdParams {
     int Hq;
     __nv_bfloat16* o;
     float* lse;
+    int64_t T_cap;
     float scale_log2;
     int* status;
     int* sched;       // global unit counter (zeroed by the plan kernel)
@@ -484,7 +485,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!xwait()) { ok = false; break; }
             const float ltot = l + xs[(1 - part) * 128 + r];
             const float inv = 1.0f / ltot;
-            const bool store = r < tile.nq && own_head;
+            const bool store =
+                r < tile.nq && own_head && ZR_BOUNDS(row_pos < p.T_cap, p.status - kStatusTimeout, 10);
             __nv_bfloat16* orow = p.o + ((int64_t)row_pos * p.Hq + h) * D + (D / 2) * part;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -534,6 +536,7 @@ zr_status launch_fwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     p.Hq = a.Hq;
     p.o = static_cast<__nv_bfloat16*>(a.o);
     p.lse = a.lse;
+    p.T_cap = a.T_cap;
     p.scale_log2 = a.scale * kLog2e;
     p.status = info.status + kStatusTimeout;  // read by zr_check_status(info)
     p.sched = ws.plan.counts + 2;

@@ -544,9 +544,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(b_dqfree(hf));
             const int qlo = 64 * hf + 16 * wg;
-            if (r < D && qlo < qb.nq) {
+            const int nv = qb.nq - qlo;
+            if (r < D && qlo < qb.nq &&
+                ZR_BOUNDS(qb.q0 + qlo + min(nv, 16) <= p.T_cap, p.status - kStatusTimeout, 20)) {
                 float* dst = p.dq_accum + ((int64_t)h * p.T_cap + qb.q0 + qlo) * D + r;
-                const int nv = qb.nq - qlo;
                 if (nv >= 16) {
                     red_add_16<D>(dst, v);  // immediate offsets, no per-query arithmetic
                 } else {
@@ -689,7 +690,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // Warpgroups 0-1 write dV columns [64 wg, +64), 2-3 write scale * dK.
             if (!__all_sync(0xffffffffu, mbar_wait(b_kempty, k & 1, ab, 40))) { ok = false; break; }
             tc_fence_after();
-            const bool store = r < t.nk;
+            const bool store = r < t.nk && ZR_BOUNDS(key_pos < p.T_cap, p.status - kStatusTimeout, 21);
             const bool is_k = wg >= 2;
             const int c0 = 64 * (wg & 1);
             const uint32_t col = (is_k ? C::kColK : C::kColV) + c0;

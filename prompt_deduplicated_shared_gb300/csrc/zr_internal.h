@@ -64,7 +64,23 @@ struct Options {
 Options& options();
 
 // device status word slots (zr_recon_info.status / attention workspace)
-enum StatusSlot { kStatusMask = 0, kStatusCapacity = 1, kStatusTimeout = 2 };
+enum StatusSlot { kStatusMask = 0, kStatusCapacity = 1, kStatusTimeout = 2, kStatusBounds = 3 };
+
+// Debug bounds checks (library built with -DZR_DEBUG_BOUNDS, libzr_debug.so):
+// ZR_BOUNDS(cond, status_words, site) is `cond` and, when it fails, records
+// `site` in status word kStatusBounds (first failure wins); the caller skips
+// the access.  In the normal build it is the constant true.
+#ifdef ZR_DEBUG_BOUNDS
+#ifdef __CUDACC__
+__device__ __forceinline__ bool zr_bounds_ok(bool ok, int32_t* status_words, int site) {
+    if (!ok) atomicCAS(status_words + kStatusBounds, 0, site);
+    return ok;
+}
+#endif
+#define ZR_BOUNDS(cond, status_words, site) (::zr::zr_bounds_ok((cond), (status_words), (site)))
+#else
+#define ZR_BOUNDS(cond, status_words, site) true
+#endif
 
 // ------------------------------------------------------------- grouping
 size_t group_workspace_bytes(int B, int L);

@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const char* __restrict__
                                                         int n_entries,
                                                         const int32_t* __restrict__ total_tokens,
                                                         int64_t T_cap, int chunk_rows,
-                                                        int64_t row_bytes) {
+                                                        int64_t row_bytes, int64_t src_rows,
+                                                        int32_t* __restrict__ status) {
     extern __shared__ int64_t s_order[];
     const int64_t T = min((int64_t)total_tokens[0], T_cap);
     const int64_t* ord = order;
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const char* __restrict__
             const int64_t n = ord[3 * j + 2];
             if (d0 >= r1) break;
             const int64_t a = max(d0, r0), e = min(d0 + n, r1);
-            if (a < e && s0 >= 0)
+            if (a < e && s0 >= 0 && ZR_BOUNDS(s0 + (e - d0) <= src_rows && e <= T_cap, status, 1))
                 block_copy<false>(src + (s0 + (a - d0)) * row_bytes, dst + a * row_bytes,
                                   (e - a) * row_bytes);
         }
@@ -433,6 +434,7 @@ __global__ void __launch_bounds__(256) reconstruct_backward_kernel(const ElemT* 
             if (d0 >= r1) break;
             const int64_t a = max(d0, r0), e = min(d0 + n, r1);
             if (a >= e || s0 < 0) continue;
+            if (!ZR_BOUNDS(s0 + (e - d0) <= (int64_t)info.B * L && e <= info.T_cap, info.status, 3)) continue;
             const int rep = (int)(s0 / L);
             const int64_t col = s0 - (int64_t)rep * L + (a - d0);  // row offset inside each member's row
             int mb = 0, me = 1;
@@ -441,6 +443,7 @@ __global__ void __launch_bounds__(256) reconstruct_backward_kernel(const ElemT* 
                 const int g = info.group_of[rep];
                 mb = info.group_ptr[g];
                 me = info.group_ptr[g + 1];
+                if (!ZR_BOUNDS(mb >= 0 && mb < me && me <= info.B, info.status, 4)) continue;
             }
             const int64_t nel = (e - a) * W;
             ElemT* dst = gpacked + a * W;
@@ -518,7 +521,7 @@ __global__ void __launch_bounds__(256) reconstruct_rows_kernel(const char* __res
         const int g = info.group_of[info.members[q]];
         const int base = info.group_ptr[g];
         const int n = info.group_ptr[g + 1] - base;
-        if (n <= 0) continue;
+        if (n <= 0 || !ZR_BOUNDS(base >= 0 && base + n <= info.B, info.status, 5)) continue;
         const int64_t local = k - (int64_t)base * nchunks;
         const int64_t c = local / n;
         const int b = info.members[base + (int)(local % n)];
@@ -531,7 +534,7 @@ __global__ void __launch_bounds__(256) reconstruct_rows_kernel(const char* __res
             const int64_t src = (kPackAdjoint && sgi == 0 && !rep) ? -1 : seg[0];
             const int64_t lo = seg[1] - row0, nrows = seg[2];
             const int64_t a = max(lo, r0), e = min(lo + nrows, r1);
-            if (a >= e) continue;
+            if (a >= e || !ZR_BOUNDS(src < 0 || src + (e - lo) <= info.T_cap, info.status, 2)) continue;
             block_copy<true>(src >= 0 ? packed + (src + (a - lo)) * row_bytes : nullptr,
                              out + (row0 + a) * row_bytes, (e - a) * row_bytes);
         }
@@ -562,7 +565,7 @@ __global__ void __launch_bounds__(256) reconstruct_pack_backward_kernel(const El
         const int g = info.group_of[info.members[q]];
         const int base = info.group_ptr[g];
         const int n = info.group_ptr[g + 1] - base;
-        if (n <= 0) continue;
+        if (n <= 0 || !ZR_BOUNDS(base >= 0 && base + n <= info.B, info.status, 6)) continue;
         const int64_t local = k - (int64_t)base * nchunks;
         const int64_t c = local / n;
         const int b = info.members[base + (int)(local % n)];
@@ -720,11 +723,11 @@ zr_status launch_pack_gather(const zr_recon_info& info, const void* src, int64_t
     if (n_entries <= kCachedPackEntries) {
         pack_rows_kernel<true><<<grid, 256, (size_t)n_entries * 24, s>>>(
             static_cast<const char*>(src), static_cast<char*>(dst), info.pack_order, n_entries,
-            info.total_tokens, info.T_cap, chunk_rows, row_bytes);
+            info.total_tokens, info.T_cap, chunk_rows, row_bytes, (int64_t)info.B * info.L, info.status);
     } else {
         pack_rows_kernel<false><<<grid, 256, 0, s>>>(
             static_cast<const char*>(src), static_cast<char*>(dst), info.pack_order, n_entries,
-            info.total_tokens, info.T_cap, chunk_rows, row_bytes);
+            info.total_tokens, info.T_cap, chunk_rows, row_bytes, (int64_t)info.B * info.L, info.status);
     }
     ZR_LAUNCH_CHECK("pack_rows_kernel");
     return ZR_OK;

@@ -16,7 +16,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libzr.so")
+# ZR_LIBRARY selects another in-tree build of the same ABI, e.g. the
+# bounds-checking libzr_debug.so (build(debug_bounds=True))
+LIB_PATH = os.environ.get("ZR_LIBRARY") or os.path.join(_HERE, "libzr.so")
 
 ZR_OK = 0
 ZR_ERR_INVALID_ARG = 1
@@ -73,6 +75,7 @@ def lib():
     sigs = {
         "zr_last_error": (ctypes.c_char_p, []),
         "zr_version": (ctypes.c_int, []),
+        "zr_debug_bounds": (ctypes.c_int, []),
         "zr_kernel_launches": (_i64, []),
         "zr_set_option": (ctypes.c_int, [ctypes.c_char_p, _i64]),
         "zr_kernel_time": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
@@ -162,6 +165,11 @@ def set_option(name: str, value: int):
 
 def version() -> int:
     return lib().zr_version()
+
+
+def debug_bounds() -> bool:
+    """True when the loaded library is the bounds-checking debug build."""
+    return lib().zr_debug_bounds() != 0
 
 
 def kernel_launches() -> int:
