@@ -123,3 +123,30 @@ def test_binding_refuses_cpu_tensors(zr):
     import torch
     with pytest.raises(ValueError, match="CUDA tensors only"):
         zr.find_prompt_groups(torch.zeros((2, 4), dtype=torch.int64), 1)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """The binding has no fallback: without the compiled library it raises."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("from prompt_deduplicated_shared_gb300 import zr\n"
+            "try:\n    zr.lib()\nexcept ImportError as e:\n    print('IMPORT_ERROR', e)\n")
+    env = dict(os.environ, ZR_LIBRARY=str(tmp_path / "missing" / "libzr.so"))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert "IMPORT_ERROR" in r.stdout
+
+
+def test_product_code_never_touches_the_oracle():
+    """The package (binding, build script, CUDA sources) names no oracle module."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = os.path.join(root, "prompt_deduplicated_shared_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\b(import|from)\s+oracle\b", text), f
+                assert "oracle/" not in text, f
