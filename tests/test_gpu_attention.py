@@ -67,6 +67,10 @@ DENSE = [
     ("bf16-leftpad-unpad", 2, 2, 190, 60, 8, 2, 64, torch.bfloat16, (1, 60), (1, 70), True),
     ("bf16-no-prompt", 1, 3, 0, 200, 2, 1, 128, torch.bfloat16, None, None, False),
     ("bf16-no-response", 2, 1, 333, 0, 2, 1, 128, torch.bfloat16, None, None, False),
+    ("bf16-d128-ratio4", 2, 2, 260, 120, 8, 2, 128, torch.bfloat16, (1, 120), None, False),
+    ("bf16-d64-ratio8", 2, 2, 300, 90, 8, 1, 64, torch.bfloat16, (1, 90), None, False),
+    ("bf16-many-groups-unpad", 5, 3, 100, 40, 4, 2, 128, torch.bfloat16, (1, 40), None, True),
+    ("bf16-long-prompt", 1, 2, 700, 150, 2, 1, 128, torch.bfloat16, (1, 150), None, False),
 ]
 
 
