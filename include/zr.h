@@ -362,7 +362,7 @@ zr_status zr_batch_stats_compute(const uint8_t* attention_mask, int B, int L, in
  *  softmax_scale <= 0 selects 1/sqrt(D)
  *  workspace     zr_split_attn_workspace(info, Hq, Hkv, D) bytes, 256-aligned;
  *                it includes the backward's fp32 dQ accumulator
- *                (T_cap * Hq * D * 4 bytes)
+ *                (T_cap rounded up to 4, times Hq * D * 4 bytes)
  * The backward takes o and lse from the forward and recomputes the attention
  * probabilities from lse.  Its dQ sums fp32 partials from different key
  * tiles in arrival order, so the last bits of dq can differ between runs;

@@ -194,7 +194,8 @@ size_t attn_workspace_layout(const zr_recon_info& info, int Hq, int D, void* bas
     w.delta = static_cast<float*>(take(sizeof(float) * (size_t)info.T_cap * Hq));
     w.lse_delta = static_cast<float2*>(take(sizeof(float2) * (size_t)lse_delta_pitch(info.T_cap) * Hq));
     // fp32 dQ accumulator of the tensor-core backward, [Hq, T_cap, D]
-    w.dq_accum = D > 0 ? static_cast<float*>(take(sizeof(float) * (size_t)info.T_cap * Hq * D)) : nullptr;
+    w.dq_accum = D > 0 ? static_cast<float*>(take(sizeof(float) * (size_t)lse_delta_pitch(info.T_cap) * Hq * D))
+                       : nullptr;
     w.bytes = off;
     if (ws) *ws = w;
     return off;

@@ -69,19 +69,58 @@ template <int kOffBytes>
 __device__ __forceinline__ void red_add_f32_at(float* base, float v) {
     asm volatile("red.global.add.f32 [%0+%2], %1;" ::"l"(base), "f"(v), "n"(kOffBytes) : "memory");
 }
-// v[j] into base[j * kStride], j = 0..15
-template <int kStride, int J = 0>
-__device__ __forceinline__ void red_add_16(float* base, const uint32_t (&v)[16]) {
-    if constexpr (J < 16) {
-        red_add_f32_at<J * kStride * 4>(base, __uint_as_float(v[J]));
-        red_add_16<kStride, J + 1>(base, v);
+template <int kOffBytes>
+__device__ __forceinline__ void red_add_v2_at(float* base, uint32_t a, uint32_t b) {
+    asm volatile("red.global.add.v2.f32 [%0+%3], {%1, %2};" ::"l"(base), "f"(__uint_as_float(a)),
+                 "f"(__uint_as_float(b)), "n"(kOffBytes) : "memory");
+}
+template <int kOffBytes>
+__device__ __forceinline__ void red_add_v4_at(float* base, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("red.global.add.v4.f32 [%0+%5], {%1, %2, %3, %4};" ::"l"(base), "f"(__uint_as_float(a)),
+                 "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d)), "n"(kOffBytes)
+                 : "memory");
+}
+// 16 consecutive queries of one head-dimension element into the interleaved
+// accumulator ([groups of 4 queries][D][4]): g0 points at slot 0 of the group
+// holding the first query, which sits in slot O.  Whole groups take one
+// 16-byte reduction (a warp's 32 elements: 512 contiguous bytes), the partial
+// groups at both ends 8- and 4-byte ones.
+template <int D, int O>
+__device__ __forceinline__ void red_add_run16(float* g0, const uint32_t (&v)[16]) {
+    constexpr int kG = 16 * D;  // bytes between consecutive groups
+    if constexpr (O == 0) {
+        red_add_v4_at<0>(g0, v[0], v[1], v[2], v[3]);
+        red_add_v4_at<kG>(g0, v[4], v[5], v[6], v[7]);
+        red_add_v4_at<2 * kG>(g0, v[8], v[9], v[10], v[11]);
+        red_add_v4_at<3 * kG>(g0, v[12], v[13], v[14], v[15]);
+    } else if constexpr (O == 1) {
+        red_add_f32_at<4>(g0, __uint_as_float(v[0]));
+        red_add_v2_at<8>(g0, v[1], v[2]);
+        red_add_v4_at<kG>(g0, v[3], v[4], v[5], v[6]);
+        red_add_v4_at<2 * kG>(g0, v[7], v[8], v[9], v[10]);
+        red_add_v4_at<3 * kG>(g0, v[11], v[12], v[13], v[14]);
+        red_add_f32_at<4 * kG>(g0, __uint_as_float(v[15]));
+    } else if constexpr (O == 2) {
+        red_add_v2_at<8>(g0, v[0], v[1]);
+        red_add_v4_at<kG>(g0, v[2], v[3], v[4], v[5]);
+        red_add_v4_at<2 * kG>(g0, v[6], v[7], v[8], v[9]);
+        red_add_v4_at<3 * kG>(g0, v[10], v[11], v[12], v[13]);
+        red_add_v2_at<4 * kG>(g0, v[14], v[15]);
+    } else {
+        red_add_f32_at<12>(g0, __uint_as_float(v[0]));
+        red_add_v4_at<kG>(g0, v[1], v[2], v[3], v[4]);
+        red_add_v4_at<2 * kG>(g0, v[5], v[6], v[7], v[8]);
+        red_add_v4_at<3 * kG>(g0, v[9], v[10], v[11], v[12]);
+        red_add_v2_at<4 * kG>(g0, v[13], v[14]);
+        red_add_f32_at<4 * kG + 8>(g0, __uint_as_float(v[15]));
     }
 }
 
 // Pairs (-LSE * log2(e), Delta = rowsum(dO * O)), head-major [Hq, pitch, 2]:
 // rows < T from the forward, rows [T, T_cap) zero (they are only read for
 // query columns that the backward masks).  The fp32 dQ accumulator ([Hq,
-// T_cap, D], head-major) of rows < T is zeroed.
+// pitch / 4, D, 4]: four consecutive queries interleaved per head-dimension
+// element) is zeroed for the query groups that hold rows < T.
 __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                      const float* __restrict__ lse, const int32_t* __restrict__ total_tokens,
                                      int64_t T_cap, int64_t pitch, int Hq, int D, float2* __restrict__ lse_delta,
@@ -104,11 +143,19 @@ __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const 
             s += __uint_as_float(xs[i] << 16) * __uint_as_float(ys[i] << 16);
             s += __uint_as_float(xs[i] & 0xffff0000u) * __uint_as_float(ys[i] & 0xffff0000u);
         }
-        const int64_t t = row / Hq;
-        const int64_t h = row - t * Hq;
-        float4* acc = reinterpret_cast<float4*>(dq_accum + (h * T_cap + t) * D) + 2 * part;
-        acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // zero the accumulator: head h's groups [0, ceil(T / 4)) are 4 * D floats
+    // each, contiguous; this thread's index covers two 16-byte vectors
+    {
+        const int64_t G4 = (T + 3) >> 2;
+        const int64_t per_head = G4 * D / 2;  // vector pairs per head
+        if (tid < per_head * Hq) {
+            const int64_t h = tid / per_head;
+            const int64_t k = tid - h * per_head;
+            float4* acc = reinterpret_cast<float4*>(dq_accum + h * pitch * D) + 2 * k;
+            acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     // reduce over the row's lanes (groups of G consecutive lanes, G a power of two)
     for (int off = G >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -119,26 +166,39 @@ __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const 
     }
 }
 
-// dQ [T, Hq, D] = scale * accumulator [Hq, T_cap, D], bf16, rows < T; eight
-// values per thread (a row of D values is contiguous on both sides)
+// dQ [T, Hq, D] = scale * accumulator [Hq, pitch / 4, D, 4], bf16, rows < T.
+// A thread takes one group of four queries and eight head-dimension elements:
+// 128 contiguous accumulator bytes in, four 16-byte bf16 rows out
+__device__ __forceinline__ float comp4(const float4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
 __global__ void attn_dq_convert_kernel(const float* __restrict__ dq_accum, const int32_t* __restrict__ total_tokens,
-                                       int64_t T_cap, int Hq, int D, float scale, __nv_bfloat16* __restrict__ dq) {
+                                       int64_t T_cap, int64_t pitch, int Hq, int D, float scale,
+                                       __nv_bfloat16* __restrict__ dq) {
     const int d8 = D / 8;
-    const int64_t n8 = min((int64_t)total_tokens[0], T_cap) * Hq * d8;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = i / d8;  // token-major (t, h)
-        const int c = (int)(i - row * d8);
-        const int64_t t = row / Hq;
-        const int64_t h = row - t * Hq;
-        const float4* src = reinterpret_cast<const float4*>(dq_accum + (h * T_cap + t) * D) + 2 * c;
-        const float4 a = __ldcs(src);
-        const float4 b = __ldcs(src + 1);
-        uint4 w;
-        w.x = pack_bf16x2(a.x * scale, a.y * scale);
-        w.y = pack_bf16x2(a.z * scale, a.w * scale);
-        w.z = pack_bf16x2(b.x * scale, b.y * scale);
-        w.w = pack_bf16x2(b.z * scale, b.w * scale);
-        reinterpret_cast<uint4*>(dq)[i] = w;
+    const int64_t T = min((int64_t)total_tokens[0], T_cap);
+    const int64_t G4 = (T + 3) >> 2;
+    const int64_t n = (int64_t)Hq * G4 * d8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t hg = i / d8;  // (head, group), head-major
+        const int c = (int)(i - hg * d8);
+        const int64_t h = hg / G4;
+        const int64_t g = hg - h * G4;
+        const float4* src = reinterpret_cast<const float4*>(dq_accum + ((h * (pitch >> 2) + g) * D + 8 * c) * 4);
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = __ldcs(src + k);
+#pragma unroll
+        for (int qi = 0; qi < 4; ++qi) {
+            const int64_t t = 4 * g + qi;
+            if (t >= T) break;
+            uint4 w;
+            w.x = pack_bf16x2(comp4(v[0], qi) * scale, comp4(v[1], qi) * scale);
+            w.y = pack_bf16x2(comp4(v[2], qi) * scale, comp4(v[3], qi) * scale);
+            w.z = pack_bf16x2(comp4(v[4], qi) * scale, comp4(v[5], qi) * scale);
+            w.w = pack_bf16x2(comp4(v[6], qi) * scale, comp4(v[7], qi) * scale);
+            *reinterpret_cast<uint4*>(dq + (t * Hq + h) * D + 8 * c) = w;
+        }
     }
 }
 
@@ -154,7 +214,8 @@ struct BwdParams {
     int64_t T_cap;
     const float2* lse_delta;  // [Hq, ld_pitch] (-LSE * log2(e), Delta)
     int64_t ld_pitch;
-    float* dq_accum;   // [Hq, T_cap, D] fp32: consecutive queries of a head are D floats apart
+    float* dq_accum;   // [Hq, pitch / 4, D, 4] fp32: four consecutive queries per element
+    int64_t acc_groups;  // pitch / 4: query groups per head
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     float scale;
@@ -547,13 +608,22 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const int nv = qb.nq - qlo;
             if (r < D && qlo < qb.nq &&
                 ZR_BOUNDS(qb.q0 + qlo + min(nv, 16) <= p.T_cap, p.status - kStatusTimeout, 20)) {
-                float* dst = p.dq_accum + ((int64_t)h * p.T_cap + qb.q0 + qlo) * D + r;
+                // element (query q, row r) of head h sits at group q / 4, slot q % 4
+                const int q = qb.q0 + qlo;  // first of the 16 query columns
+                float* head = p.dq_accum + ((int64_t)h * p.acc_groups * D + r) * 4;
                 if (nv >= 16) {
-                    red_add_16<D>(dst, v);  // immediate offsets, no per-query arithmetic
+                    float* g0 = head + (int64_t)(q >> 2) * D * 4;
+                    switch (q & 3) {  // warp-uniform
+                        case 0: red_add_run16<D, 0>(g0, v); break;
+                        case 1: red_add_run16<D, 1>(g0, v); break;
+                        case 2: red_add_run16<D, 2>(g0, v); break;
+                        default: red_add_run16<D, 3>(g0, v); break;
+                    }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (j < nv) red_add_f32(dst + j * D, __uint_as_float(v[j]));
+                        if (j < nv) red_add_f32(head + (int64_t)((q + j) >> 2) * D * 4 + ((q + j) & 3),
+                                                __uint_as_float(v[j]));
                 }
             }
             return true;
@@ -740,7 +810,7 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     if (((uintptr_t)a.dq & 15) || ((uintptr_t)ws.dq_accum & 15))
         return set_error(ZR_ERR_INVALID_ARG, "dq must be 16-byte aligned");
     {
-        const int64_t threads = a.T_cap * a.Hq * (D / 8);
+        const int64_t threads = lse_delta_pitch(a.T_cap) * a.Hq * (D / 8);
         const int64_t blocks = (threads + 255) / 256;
         KernelTimer timer("attn_bwd_prep", s);
         attn_bwd_prep_kernel<<<(unsigned)blocks, 256, 0, s>>>(
@@ -763,6 +833,7 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     p.lse_delta = ws.lse_delta;
     p.ld_pitch = lse_delta_pitch(a.T_cap);
     p.dq_accum = ws.dq_accum;
+    p.acc_groups = lse_delta_pitch(a.T_cap) / 4;
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
     p.scale = a.scale;
@@ -780,7 +851,8 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     }
     {
         KernelTimer timer("attn_dq_convert", s);
-        attn_dq_convert_kernel<<<num_sms() * 8, 256, 0, s>>>(ws.dq_accum, info.total_tokens, a.T_cap, a.Hq, D,
+        attn_dq_convert_kernel<<<num_sms() * 8, 256, 0, s>>>(ws.dq_accum, info.total_tokens, a.T_cap,
+                                                             lse_delta_pitch(a.T_cap), a.Hq, D,
                                                              a.scale, static_cast<__nv_bfloat16*>(a.dq));
         ZR_LAUNCH_CHECK("attn_dq_convert_kernel");
     }

@@ -157,7 +157,10 @@ struct AttnWorkspace {
     // [Hq, lse_delta_pitch(T_cap)] pairs (-LSE * log2(e), rowsum(dO * O)),
     // backward only (tensor cores)
     float2* lse_delta;
-    float* dq_accum;     // [Hq, T_cap, D] fp32, tensor-core backward only
+    // fp32 dQ accumulator of the tensor-core backward, [Hq, pitch / 4, D, 4]:
+    // four consecutive queries interleaved per head-dimension element
+    // (pitch = lse_delta_pitch(T_cap))
+    float* dq_accum;
     size_t bytes;
 };
 
