@@ -187,7 +187,7 @@ __global__ void attn_dq_convert_kernel(const float* __restrict__ dq_accum, const
         const float4* src = reinterpret_cast<const float4*>(dq_accum + ((h * (pitch >> 2) + g) * D + 8 * c) * 4);
         float4 v[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = __ldcs(src + k);
+        for (int k = 0; k < 8; ++k) v[k] = __ldg(src + k);
 #pragma unroll
         for (int qi = 0; qi < 4; ++qi) {
             const int64_t t = 4 * g + qi;
