@@ -124,12 +124,20 @@ def _sample_rows(info, per_segment, rng):
     return sorted(set(t for t in rows if info.row_valid[t]))
 
 
-FULL = [("qwen3_0p6b", False), ("worked_example", False), ("pipeline", False), ("pipeline", True),
-        ("pipeline_nodedup", False), ("long_context", False)]
+# (workload, use_unpad, heads): heads overrides (Hq, Hkv, D) of the workload to
+# run the same batch through another kernel configuration (head_dim 64, GQA 4)
+FULL = [("qwen3_0p6b", False, None), ("worked_example", False, None), ("pipeline", False, None),
+        ("pipeline", True, None), ("pipeline_nodedup", False, None), ("long_context", False, None),
+        ("worked_example", False, (16, 4, 64))]
 
 
-@pytest.mark.parametrize("wname,use_unpad", FULL, ids=[f"{w}-{'unpad' if u else 'pad'}" for w, u in FULL])
-def test_full_size_sampled(zr, wname, use_unpad):
+def _full_id(c):
+    w, u, hd = c
+    return f"{w}-{'unpad' if u else 'pad'}" + ("" if hd is None else f"-h{hd[0]}-{hd[1]}-d{hd[2]}")
+
+
+@pytest.mark.parametrize("wname,use_unpad,heads", FULL, ids=[_full_id(c) for c in FULL])
+def test_full_size_sampled(zr, wname, use_unpad, heads):
     """Every configuration at full size, in the launch configuration the bench
     uses: the forward on sampled query rows of every prompt and response, the
     backward with the upstream gradient zero outside a sampled row set (the
@@ -140,7 +148,8 @@ def test_full_size_sampled(zr, wname, use_unpad):
     _, _, _, _, info_ref = oracle_pack(ids, mask, pos, wl.R, use_unpad)
     _, _, _, _, info, T = gpu_pack(zr, ids, mask, pos, wl.R, use_unpad, T_cap=info_ref.T)
     assert T == info_ref.T
-    (q, k, v, do), (tq, tk, tv, tdo) = qkv_inputs(T, wl.Hq, wl.Hkv, wl.D, 100 + idx, torch.bfloat16)
+    Hq, Hkv, D = heads if heads is not None else (wl.Hq, wl.Hkv, wl.D)
+    (q, k, v, do), (tq, tk, tv, tdo) = qkv_inputs(T, Hq, Hkv, D, 100 + idx, torch.bfloat16)
     rng = np.random.default_rng(idx + (50 if use_unpad else 0))
     per = 2 if wname in ("long_context", "pipeline_nodedup") else 6
     rows = _sample_rows(info_ref, per, rng)
