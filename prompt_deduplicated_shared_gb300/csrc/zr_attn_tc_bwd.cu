@@ -16,13 +16,15 @@
 //                            the query blocks that see them (all query heads of
 //                            the group) stream through a TMA ring of 64-query
 //                            halves (with the half's block descriptor and its
-//                            LSE/Delta pairs); per half, S^T = K Q^T and dP^T = V dO^T go
-//                            to TMEM, the softmax warps write P^T and dS^T back
+//                            -LSE/Delta, staged by the producer warp); per half,
+//                            S^T = K Q^T and dP^T = V dO^T go to TMEM, the
+//                            softmax warps write P^T and dS^T back
 //                            to TMEM (bf16) and dS to shared memory, then
 //                            dV += P^T dO, dK += dS^T Q (A operands from TMEM)
 //                            and dQ^T = K^T dS^T (a per-half partial) run on the
 //                            tensor cores; the softmax warps add each dQ^T
-//                            partial into the fp32 accumulator (red.global.add)
+//                            partial into the fp32 accumulator (16-byte
+//                            red.global.add.v4 into groups of four queries)
 //   attn_dq_convert_kernel   dQ = scale * accumulator, rounded to bf16
 // The query blocks that see a prompt key tile are the prompt's own blocks
 // from the diagonal on (causal) and every block of every response of the
