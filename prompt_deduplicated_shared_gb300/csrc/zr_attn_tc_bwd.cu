@@ -58,6 +58,16 @@ __device__ __forceinline__ void st_shared_v4_nc(uint32_t addr, uint32_t a, uint3
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
+// 3-D tiled TMA load (x innermost)
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v2(uint32_t addr, float a, float b) {
     asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
@@ -448,12 +458,9 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                             (uint32_t)h, qb.diag ? 1u : 0u);
                             mbar_expect_tx(b_qfull(slot), 2 * C::kHalf);
                             const uint32_t qb_s = sQD + slot * 2 * C::kHalf;
-#pragma unroll
-                            for (int c = 0; c < C::kChunks; ++c) {
-                                tma_load_2d(qb_s + c * C::kHalfChunk, &tm_q, h * D + 64 * c, row, b_qfull(slot));
-                                tma_load_2d(qb_s + C::kHalf + c * C::kHalfChunk, &tm_do, h * D + 64 * c, row,
-                                            b_qfull(slot));
-                            }
+                            // one box per tensor: 64 rows x the head's kChunks column chunks
+                            tma_load_3d(qb_s, &tm_q, 0, row, h * C::kChunks, b_qfull(slot));
+                            tma_load_3d(qb_s + C::kHalf, &tm_do, 0, row, h * C::kChunks, b_qfull(slot));
                         }
                         ++qstage;
                     }
@@ -804,9 +811,25 @@ zr_status launch_bwd(const zr_recon_info& info, const AttnWorkspace& ws, const A
     using C = BwdCfg<D>;
     CUtensorMap tq, tk, tv, tdo;
     zr_status st;
-    // Q and dO: 64-row boxes (the kernel stages them per 64-query half)
-    if ((st = make_map(&tq, a.q, (int64_t)a.Hq * D, a.T_cap, (int64_t)a.Hq * D * 2, 64)) != ZR_OK) return st;
-    if ((st = make_map(&tdo, a.dout, (int64_t)a.Hq * D, a.T_cap, (int64_t)a.Hq * D * 2, 64)) != ZR_OK) return st;
+    // Q and dO: [64-column chunk, row, chunk index] views, boxes of 64 rows x
+    // the kChunks chunks of one head (the kernel stages them per 64-query
+    // half, chunk-major, 128-byte swizzle)
+    for (int w = 0; w < 2; ++w) {
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return set_error(ZR_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+        const void* base = w == 0 ? a.q : a.dout;
+        const int64_t row_bytes = (int64_t)a.Hq * D * 2;
+        if (((uintptr_t)base & 15) || (row_bytes & 15))
+            return set_error(ZR_ERR_INVALID_ARG, "q/k/v must be 16-byte aligned with 16-byte row strides");
+        cuuint64_t dims[3] = {64, (cuuint64_t)a.T_cap, (cuuint64_t)(a.Hq * D / 64)};
+        cuuint64_t strides[2] = {(cuuint64_t)row_bytes, 128};
+        cuuint32_t box[3] = {64, 64, (cuuint32_t)C::kChunks};
+        cuuint32_t estr[3] = {1, 1, 1};
+        const CUresult r = fn(w == 0 ? &tq : &tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return set_error(ZR_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
     if ((st = make_map(&tk, a.k, (int64_t)a.Hkv * D, a.T_cap, (int64_t)a.Hkv * D * 2)) != ZR_OK) return st;
     if ((st = make_map(&tv, a.v, (int64_t)a.Hkv * D, a.T_cap, (int64_t)a.Hkv * D * 2)) != ZR_OK) return st;
     if (((uintptr_t)a.dq & 15) || ((uintptr_t)ws.dq_accum & 15))
