@@ -318,8 +318,8 @@ constexpr int kBwdThreads = 576;
 // Each 128-query block is processed as two 64-query halves A and B with their
 // own TMEM columns, so that one half's softmax overlaps the other half's GEMMs.
 // MMA order per block `it` (waits in brackets):
-//   S^T_A | [dQ^T_A(it-1) read out] dP^T_A | [softmax B(it-1)] dV, dK, dQ^T of B(it-1)
-//   | S^T_B | [dQ^T_B(it-1) read out] dP^T_B | [softmax A(it)] dV, dK, dQ^T of A(it)
+//   S^T_A | [dQ^T_A(it-1) read out] dP^T_A | [softmax B(it-1)] dQ^T, dV, dK of B(it-1)
+//   | S^T_B | [dQ^T_B(it-1) read out] dP^T_B | [softmax A(it)] dQ^T, dV, dK of A(it)
 // The softmax warps run: softmax A(it) | read out dQ^T_B(it-1) | softmax B(it)
 // | read out dQ^T_A(it).  The four warpgroups take 16 query columns of a half
 // each (warpgroup g: columns [16 g, +16)); a warpgroup writes P^T and dS^T
@@ -524,13 +524,21 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (leader) mma_commit(b_dpfull(h));
             return true;
         };
-        // once the softmax wrote half h: dV += P^T_h dO_h, dK += dS^T_h Q_h (A
-        // operands from TMEM; first = overwrite), dQ^T_h = K^T dS^T_h (B from
-        // shared memory) into the dP^T columns
+        // once the softmax wrote half h: dQ^T_h = K^T dS^T_h (B from shared
+        // memory) into the dP^T columns, then dV += P^T_h dO_h and dK += dS^T_h
+        // Q_h (A operands from TMEM; first = overwrite)
         auto issue_acc = [&](int slot, int h, bool first) -> bool {
             if (!wait(b_pdsfull(h), pds_cnt[h] & 1, 35)) return false;
             ++pds_cnt[h];
             tc_fence_after();
+            // dQ^T first, so that its read-out (which frees the dP^T columns for
+            // the next block) overlaps the dV and dK GEMMs
+            const uint64_t dds0 = smem_desc(sDS + h * C::kDS, C::kDS, 1024);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                if (leader) mma_bf16_ss(tmem + C::col_p(h), dKt0 + s * 128, dds0 + s * 128, idesc_dq, s > 0 ? 1u : 0u);
+            if (leader) mma_commit(b_dqfull(h));
+            ++dq_cnt[h];
             const uint32_t qh = sQD + slot * 2 * C::kHalf, dh = qh + C::kHalf;
             const uint64_t bq0 = smem_desc(qh, C::kHalfChunk, 1024), bdo0 = smem_desc(dh, C::kHalfChunk, 1024);
 #pragma unroll
@@ -541,12 +549,6 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int s = 0; s < 4; ++s)
                 if (leader) mma_bf16_ts(tmem + C::kColK, tmem + C::col_s(h) + 16 * s + 8, bq0 + s * 128, idesc_acc,
                                         (!first || s > 0) ? 1u : 0u);
-            const uint64_t dds0 = smem_desc(sDS + h * C::kDS, C::kDS, 1024);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                if (leader) mma_bf16_ss(tmem + C::col_p(h), dKt0 + s * 128, dds0 + s * 128, idesc_dq, s > 0 ? 1u : 0u);
-            if (leader) mma_commit(b_dqfull(h));
-            ++dq_cnt[h];
             return true;
         };
         for (; ok; ++k) {
