@@ -720,7 +720,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     uint32_t dr[16];
                     tmem_ld16(trow + C::col_p(hf) + 16 * wg, dr);
                     tmem_wait_ld();
-                    uint32_t pk[8], dk[8];
+                    uint32_t pd[16];  // P^T (8 bf16 pairs), then dS^T (8 pairs)
 #pragma unroll
                     for (int pc = 0; pc < 8; ++pc) {
                         // dS = P * (dP - Delta), two columns per instruction (the
@@ -731,20 +731,19 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                          f2_sub(f2_pack(__uint_as_float(dr[2 * pc]), __uint_as_float(dr[2 * pc + 1])),
                                                 (pc & 1) ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y))),
                                   ds[0], ds[1]);
-                        pk[pc] = pack_bf16x2(pv[2 * pc], pv[2 * pc + 1]);
-                        dk[pc] = pack_bf16x2(ds[0], ds[1]);
+                        pd[pc] = pack_bf16x2(pv[2 * pc], pv[2 * pc + 1]);
+                        pd[8 + pc] = pack_bf16x2(ds[0], ds[1]);
                     }
-                    // P^T and dS^T (bf16 pairs) over the 16 S^T columns read
-                    tmem_st8(trow + C::col_s(hf) + 16 * wg, pk);
-                    tmem_st8(trow + C::col_s(hf) + 16 * wg + 8, dk);
+                    // P^T and dS^T (bf16 pairs) over the 16 S^T columns read, one store
+                    tmem_st16(trow + C::col_s(hf) + 16 * wg, pd);
                     // dS into shared memory, key row r, query columns [16 wg, +16):
                     // 16-byte pieces 2 wg and 2 wg + 1 of the row, 128-byte swizzle.
                     // The previous dQ^T of this half, which read the buffer, has
                     // completed: its result was read out before this half began.
                     {
                         const uint32_t row = sDS + hf * C::kDS + (r >> 3) * 1024 + (r & 7) * 128;
-                        st_shared_v4_nc(row + (((2 * wg) ^ (r & 7)) << 4), dk[0], dk[1], dk[2], dk[3]);
-                        st_shared_v4_nc(row + (((2 * wg + 1) ^ (r & 7)) << 4), dk[4], dk[5], dk[6], dk[7]);
+                        st_shared_v4_nc(row + (((2 * wg) ^ (r & 7)) << 4), pd[8], pd[9], pd[10], pd[11]);
+                        st_shared_v4_nc(row + (((2 * wg + 1) ^ (r & 7)) << 4), pd[12], pd[13], pd[14], pd[15]);
                     }
                     fence_async_smem();
                     tmem_wait_st();
